@@ -1,0 +1,420 @@
+"""Benchmark of the preshuffled-weight GEMM on GB300.
+
+Default workload: the FP8 e4m3 per-tensor split-K decode sweep the pages
+measure (M in {1,16} x N in {2048,16384}, K=7168; split_k from the dispatch
+table), one step = the four GEMMs (mainloop + split-K reduce) back to back.
+Metric: decode GEMM GB/s = algorithmic bytes (A + B + scales + Y) / time,
+whole job over all ranks.  Other workloads: --workload (see WORKLOADS).
+
+Prints one JSON line (rank 0).  ``--impl reference`` times the CPU oracle on
+the host cores instead (a bounded sample of the same workload per step).
+"""
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import inputs  # noqa: E402
+
+PEAKS_FILE = os.path.join(ROOT, "MEASURED_PEAKS.json")
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+# ---------------------------------------------------------------- workloads
+
+def decode_cases(mode, K=7168):
+    return [dict(mode=mode, M=m, N=n, K=K) for m, n in inputs.DECODE_SHAPES]
+
+
+WORKLOADS = {
+    "fp8_tensor_decode_sweep_k7168": dict(cases=decode_cases("fp8_tensor"), kind="decode", idx=1),
+    "fp8_block128_decode_sweep_k7168": dict(cases=decode_cases("fp8_block128"), kind="decode", idx=2),
+    "mxfp8_decode_n16384_k7168": dict(cases=[dict(mode="mxfp8", M=m, N=16384, K=7168) for m in (1, 16)],
+                                      kind="decode", idx=4),
+    "mxfp4_decode_n16384_k7168": dict(cases=[dict(mode="mxfp4", M=m, N=16384, K=7168) for m in (1, 16)],
+                                      kind="decode", idx=4),
+}
+DEFAULT_WORKLOAD = "fp8_tensor_decode_sweep_k7168"
+
+
+def elem_bytes(mode):
+    return {"bf16": 2.0, "mxfp4": 0.5}.get(mode, 1.0)
+
+
+def scale_bytes(mode, M, N, K):
+    if mode == "fp8_tensor":
+        return 8
+    if mode == "fp8_block128":
+        return 4 * (M + N // 128) * (K // 128)
+    if mode == "mxfp8":
+        return (M + N) * (K // 128)
+    if mode == "mxfp4":
+        return (M + N) * (K // 32)
+    return 0
+
+
+def algo_bytes(c, n=None):
+    """A + B + scales + Y bytes of one GEMM (n restricts to the first n weight rows)."""
+    M, N, K, mode = c["M"], c["N"] if n is None else n, c["K"], c["mode"]
+    return int(M * K * elem_bytes(mode) + N * K * elem_bytes(mode) + scale_bytes(mode, M, N, K) + 2 * M * N)
+
+
+def case_operands(wl_idx, i, c):
+    off = 10 * i
+    return inputs.operands(c["mode"], c["M"], c["N"], c["K"], 1000 + wl_idx + off, 2000 + wl_idx + off,
+                           3000 + wl_idx + off)
+
+
+# ------------------------------------------------------------------ clocks
+
+class ClockSampler:
+    """Samples nvidia-smi SM clocks and throttle reasons in the background."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index, self.proc, self.lines = index, None, []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.index), "--query-gpu=" + self.FIELDS,
+                                          "--format=csv,noheader,nounits", "-lms", "50"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except (OSError, ValueError):
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.thread.join(timeout=2)
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 7:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                smax.append(float(parts[1]))
+            except ValueError:
+                continue
+            for nm, v in zip(names, parts[3:7]):
+                if v.lower() in ("active", "1", "yes"):
+                    reasons.add(nm)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ------------------------------------------------------------- oracle arm
+
+class OracleSample:
+    """The oracle on a sample of each case: the first n weight rows (all M rows,
+    full K), n the same fraction of N for every case, calibrated once so that
+    one pass costs about target_s seconds."""
+
+    def __init__(self, wl, host_ops, target_s):
+        import oracle
+        self.oracle = oracle
+        self.orc = {"bf16": oracle.BF16, "fp8_tensor": oracle.FP8_TENSOR, "fp8_block128": oracle.FP8_BLOCK128,
+                    "mxfp8": oracle.MXFP8, "mxfp4": oracle.MXFP4}
+        self.wl, self.host_ops = wl, host_ops
+        self.threads = os.cpu_count() or 1
+        self.frac = 1.0 / 1024
+        t, _ = self.run()
+        self.frac = min(1.0, max(1.0 / 1024, self.frac * target_s / max(t, 1e-6)))
+
+    def rows(self, c):
+        return max(8, int(c["N"] * self.frac) // 8 * 8)
+
+    def run(self):
+        t0 = time.perf_counter()
+        nbytes = 0
+        for c, (A, B, a_s, b_s) in zip(self.wl["cases"], self.host_ops):
+            n = self.rows(c)
+            bs = b_s
+            if c["mode"] == "fp8_block128":
+                bs = b_s[: (n + 127) // 128]
+            elif c["mode"] in ("mxfp8", "mxfp4"):
+                bs = b_s[:n]
+            self.oracle.gemm(self.orc[c["mode"]], A, B[:n], a_s, bs, M=c["M"], N=n, K=c["K"],
+                             threads=self.threads)
+            nbytes += algo_bytes(c, n)
+        return time.perf_counter() - t0, nbytes
+
+    def describe(self):
+        return "first %s weight rows of the %s cases (all M rows, full K) per pass" % (
+            "/".join(str(self.rows(c)) for c in self.wl["cases"]), len(self.wl["cases"]))
+
+
+# ------------------------------------------------------------------- main
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=3000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", default="fg", choices=["fg", "reference"])
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(WORKLOADS))
+    ap.add_argument("--rotate", type=int, default=3, help="weight copies cycled to keep L2 cold")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    wl = WORKLOADS[args.workload]
+    peaks = dict(FALLBACK_PEAKS)
+    peaks_src = "fallback"
+    if os.path.exists(PEAKS_FILE):
+        try:
+            peaks.update(json.load(open(PEAKS_FILE)))
+            peaks_src = "measured"
+        except ValueError:
+            pass
+
+    if args.impl == "reference":
+        if rank != 0:
+            return
+        host_ops = [case_operands(wl["idx"], i, c) for i, c in enumerate(wl["cases"])]
+        budget = 90.0 / max(1, args.steps + args.warmup)   # whole run ~1.5 min
+        ref = OracleSample(wl, host_ops, budget)
+        times, total_bytes = [], 0
+        for s in range(args.warmup + args.steps):
+            t, nb = ref.run()
+            if s >= args.warmup:
+                times.append(t)
+                total_bytes += nb
+        tsum = sum(times)
+        value = total_bytes / tsum / 1e9
+        threads = ref.threads
+        sample = ref.describe()
+        line = {"metric": "decode GEMM GB/s", "value": value, "unit": "GB/s", "impl": "reference",
+                "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+                "ms_per_step": 1000 * tsum / len(times), "higher_is_better": True, "scaling": "weak",
+                "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+                "config": {"workload": args.workload, "cases": wl["cases"]},
+                "cpu_baseline": {"value": value, "unit": "GB/s", "cores": threads, "kind": "oracle",
+                                 "sample": sample},
+                "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+        print(json.dumps(line), flush=True)
+        return
+
+    import torch
+    import torch.distributed as dist
+
+    import mx_gemm_gb300 as fg
+
+    if world > 1:
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+
+    def to_dev(x):
+        if x is None:
+            return None
+        x = np.ascontiguousarray(x)
+        return torch.from_numpy(x.view(np.int16) if x.dtype == np.uint16 else x).to(dev)
+
+    # operands: one activation per case, `rotate` preshuffled copies of each weight
+    host_ops = [case_operands(wl["idx"], i, c) for i, c in enumerate(wl["cases"])]
+    cases = []
+    for c, (A, B, a_s, b_s) in zip(wl["cases"], host_ops):
+        dB, db_s = to_dev(B), to_dev(b_s)
+        pbs = [fg.preshuffle_b(c["mode"], dB, db_s, K=c["K"]) for _ in range(max(1, args.rotate))]
+        del dB
+        plan = fg.gemm_plan(c["mode"], c["M"], c["N"], c["K"])
+        S = plan["split_k"]
+        ws = torch.empty(max(1, S * c["M"] * c["N"]), dtype=torch.float32, device=dev)
+        Y = torch.empty((c["M"], c["N"]), dtype=torch.bfloat16, device=dev)
+        dA, da_s = to_dev(A), to_dev(a_s)
+        hA = torch.from_numpy(np.ascontiguousarray(A).view(np.int16) if A.dtype == np.uint16 else
+                              np.ascontiguousarray(A)).pin_memory()
+        ha_s = torch.from_numpy(np.ascontiguousarray(a_s)).pin_memory() if a_s is not None else None
+        hY = torch.empty((c["M"], c["N"]), dtype=torch.bfloat16).pin_memory()
+        red_as = da_s if c["mode"] == "fp8_tensor" else None
+        red_bs = pbs[0].sf[:4].view(torch.float32) if c["mode"] == "fp8_tensor" else None
+        cases.append(dict(c=c, pbs=pbs, S=S, ws=ws, Y=Y, dA=dA, da_s=da_s, hA=hA, ha_s=ha_s, hY=hY,
+                          plan=plan, bytes=algo_bytes(c), red_as=red_as, red_bs=red_bs))
+    torch.cuda.synchronize()
+
+    def one_case(x, r, ev=None):
+        st = torch.cuda.current_stream()
+        pb = x["pbs"][r % len(x["pbs"])]
+        S = x["S"]
+        if ev is not None:
+            ev[0].record(st)
+        if S > 1:
+            fg.gemm(x["dA"], pb, x["da_s"], split_k=S, Y=x["Y"], workspace=x["ws"],
+                    flags=fg.FG_FLAG_DEFER_REDUCE, stream=st)
+            if ev is not None:
+                ev[1].record(st)
+            rs = pb.sf[:4].view(torch.float32) if x["c"]["mode"] == "fp8_tensor" else None
+            fg.gemm_splitk_reduce(x["ws"], S, x["c"]["M"], x["c"]["N"], x["red_as"], rs, Y=x["Y"], stream=st)
+        else:
+            fg.gemm(x["dA"], pb, x["da_s"], split_k=1, Y=x["Y"], stream=st)
+            if ev is not None:
+                ev[1].record(st)
+
+    def step(r, evs=None):
+        for i, x in enumerate(cases):
+            one_case(x, r, None if evs is None else evs[i])
+
+    for w in range(args.warmup):
+        step(w)
+    torch.cuda.synchronize()
+    if fg.get_error() != fg.FG_OK:
+        raise RuntimeError("kernel error word set during warm-up")
+
+    # The K timed steps are captured once into a CUDA graph (a decode step is
+    # launch-bound on the host otherwise) with timing events around every
+    # mainloop launch, then replayed once inside the timed region.
+    K = args.steps
+    graph = None
+    try:
+        evs = [[[torch.cuda.Event(enable_timing=True, external=True) for _ in range(2)] for _ in cases]
+               for _ in range(K)]
+        graph = torch.cuda.CUDAGraph()
+        cap = torch.cuda.Stream()
+        cap.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.graph(graph, stream=cap):
+            for s in range(K):
+                step(s, evs[s])
+        torch.cuda.synchronize()
+        graph.replay()                      # one untimed replay
+        torch.cuda.synchronize()
+    except TypeError:
+        graph = None
+        evs = [[[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in cases] for _ in range(K)]
+    stream = torch.cuda.current_stream()
+    clk = ClockSampler(local_rank)
+    clk.start()
+    time.sleep(0.2)
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    if graph is not None:
+        graph.replay()
+    else:
+        for s in range(K):
+            step(s, evs[s])
+    t1.record(stream)
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    clocks = clk.stop()
+    ms = t0.elapsed_time(t1)
+    if world > 1:
+        tt = torch.tensor([ms], device=dev)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        ms = float(tt.item())
+    if fg.get_error() != fg.FG_OK:
+        raise RuntimeError("kernel error word set during the timed region")
+    step_bytes = sum(x["bytes"] for x in cases)
+    value = world * K * step_bytes / (ms / 1e3) / 1e9
+
+    # dominant kernel: the mainloop (decode) kernel over all cases
+    main_ms = [0.0] * len(cases)
+    for s in range(K):
+        for i in range(len(cases)):
+            main_ms[i] += evs[s][i][0].elapsed_time(evs[s][i][1])
+    per_case = []
+    for i, x in enumerate(cases):
+        avg = main_ms[i] / K
+        per_case.append({"M": x["c"]["M"], "N": x["c"]["N"], "K": x["c"]["K"], "split_k": x["S"],
+                         "kernel": x["plan"]["name"], "mainloop_us": round(avg * 1e3, 3),
+                         "mainloop_gbs": round(x["bytes"] / (avg / 1e3) / 1e9, 1)})
+    main_avg_s = sum(main_ms) / K / 1e3
+    achieved = step_bytes / main_avg_s / 1e9
+    peak = float(peaks["hbm_gbs"])
+
+    # ---------------- end-to-end: host buffers, H2D of A, D2H of Y in the region
+    E = max(3, K // 10)
+    h2d = sum(x["hA"].numel() * x["hA"].element_size() +
+              (x["ha_s"].numel() * x["ha_s"].element_size() if x["ha_s"] is not None else 0) for x in cases)
+    d2h = sum(x["hY"].numel() * x["hY"].element_size() for x in cases)
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for s in range(E):
+        for x in cases:
+            x["dA"].copy_(x["hA"], non_blocking=True)
+            if x["ha_s"] is not None:
+                x["da_s"].copy_(x["ha_s"], non_blocking=True)
+            one_case(x, s)
+            x["hY"].copy_(x["Y"], non_blocking=True)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = e0.elapsed_time(e1)
+    e2e_value = world * E * step_bytes / (e2e_ms / 1e3) / 1e9
+
+    launches_per_step = sum(2 if x["S"] > 1 else 1 for x in cases)
+
+    cpu = None
+    if rank == 0 and not args.no_cpu_baseline:
+        ref = OracleSample(wl, host_ops, 15.0)
+        t, nb = ref.run()
+        cpu = {"value": nb / t / 1e9, "unit": "GB/s", "cores": ref.threads, "kind": "oracle",
+               "sample": ref.describe() + ", one pass of %.1f s" % t}
+
+    if rank == 0:
+        line = {
+            "metric": "decode GEMM GB/s", "value": value, "unit": "GB/s", "n_gpus": world, "steps": K,
+            "warmup": args.warmup, "ms_per_step": ms / K, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "e4m3" if "fp8" in args.workload else
+            ("e2m1" if "mxfp4" in args.workload else "e4m3"),
+            "data": "synthetic",
+            "config": {"workload": args.workload, "K": 7168,
+                       "shapes": [[x["c"]["M"], x["c"]["N"]] for x in cases],
+                       "l2": "inputs larger than L2: %d distinct preshuffled weight copies, %.0f MB of weights "
+                             "per step, each weight reused only after the others" %
+                             (args.rotate * len(cases), args.rotate * sum(x["c"]["N"] * x["c"]["K"] *
+                                                                            elem_bytes(x["c"]["mode"])
+                                                                            for x in cases) / 1e6),
+                       "parallelism": "replicas" if world > 1 else "single"},
+            "per_case": per_case,
+            "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+                         "frac": round(achieved / peak, 4), "traffic": None,
+                         "peak_source": peaks_src + " hbm_gbs (burst copy)",
+                         "kernel": "decode mainloop (all cases, reduce excluded)"},
+            "cpu_baseline": cpu,
+            "e2e": {"value": e2e_value, "unit": "GB/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+            "gpu_launches": launches_per_step * K,
+            "clocks": clocks,
+            "timed_region": "one CUDA-graph replay of the %d steps" % K if graph is not None else "eager launches",
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,504 @@
+// C ABI of the preshuffled-weight GEMM library: argument and shape checks,
+// the weight descriptor, the shape-keyed dispatch table, TMA descriptor
+// set-up and kernel launches.  Host code only (plus the device error word).
+//
+// Checks follow the pages' rules: a clear, early error off the supported
+// arch (FlyDSL PR "Enable the gmem->LDS async copy for f16/bf16 preshuffle
+// GEMM", review reply on the arch guard), K must be a multiple of the scale
+// block (aiter PR "FlyDSL split-K preshuffle decode GEMM for small-M
+// shapes", Copilot review), never shuffle already-preshuffled weights (same
+// PR, last Copilot review), and refuse a tile shape the kernel cannot load
+// whole (FlyDSL PR "Migrate kernels to fx.copy / .llvm_ptr", commit
+// "Reject tiles whose A tile is only partially loaded").
+#include <cudaTypedefs.h>
+
+#include <atomic>
+#include <cstdarg>
+#include <cstdio>
+#include <cstdlib>
+#include <cstring>
+#include <mutex>
+
+#include "../../include/fg.h"
+#include "fg_internal.cuh"
+
+namespace fg {
+
+static __device__ uint32_t g_dev_error;
+
+namespace {
+
+thread_local char g_msg[512] = "";
+std::atomic<uint64_t> g_timeout_ns{4000000000ull};
+std::atomic<int> g_cc_major_override{-1}, g_cc_minor_override{0};
+
+fg_status fail(fg_status s, const char* fmt, ...) {
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(g_msg, sizeof g_msg, fmt, ap);
+  va_end(ap);
+  return s;
+}
+
+fg_status cuda_fail(cudaError_t e, const char* what) {
+  return fail(FG_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
+
+bool mode_ok(int mode) { return mode >= FG_BF16 && mode <= FG_MXFP4; }
+
+const char* mode_name(int mode) {
+  static const char* names[] = {"bf16", "fp8_tensor", "fp8_block128", "mxfp8", "mxfp4"};
+  return mode_ok(mode) ? names[mode] : "?";
+}
+
+// Shape rules shared by every call.
+fg_status check_nk(int mode, int64_t N, int64_t K) {
+  if (N <= 0 || K <= 0) return fail(FG_ERR_SHAPE, "N=%lld and K=%lld must be positive", (long long)N, (long long)K);
+  if (N % 128) return fail(FG_ERR_SHAPE, "N=%lld must be a multiple of 128", (long long)N);
+  const int64_t need = mode == FG_BF16 ? 64 : (mode == FG_MXFP4 ? 256 : 128);
+  if (K % need)
+    return fail(FG_ERR_SHAPE, "K=%lld must be a multiple of %lld for %s (whole 128-byte K slabs%s)", (long long)K,
+                (long long)need, mode_name(mode),
+                (mode == FG_FP8_BLOCK128 || mode == FG_MXFP8) ? " and whole 128-K scale blocks" : "");
+  if (N > (int64_t(1) << 24) || K > (int64_t(1) << 20))
+    return fail(FG_ERR_SHAPE, "N=%lld or K=%lld too large", (long long)N, (long long)K);
+  return FG_OK;
+}
+
+fg_status check_arch() {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  int major = g_cc_major_override.load(), minor = g_cc_minor_override.load();
+  if (major < 0) {
+    if ((e = cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev)) != cudaSuccess)
+      return cuda_fail(e, "cudaDeviceGetAttribute");
+    if ((e = cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev)) != cudaSuccess)
+      return cuda_fail(e, "cudaDeviceGetAttribute");
+  }
+  if (major != 10 || minor != 3)
+    return fail(FG_ERR_UNSUPPORTED_ARCH, "device compute capability %d.%d; this library runs on 10.3 (sm_103a) only",
+                major, minor);
+  return FG_OK;
+}
+
+// Device address of the error word, per device (looked up once each).
+uint32_t* dev_error_ptr() {
+  static std::mutex mu;
+  static uint32_t* ptrs[64] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+  std::lock_guard<std::mutex> lock(mu);
+  if (!ptrs[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_dev_error) != cudaSuccess) return nullptr;
+    ptrs[dev] = static_cast<uint32_t*>(p);
+  }
+  return ptrs[dev];
+}
+
+uint64_t fnv1a(const void* data, size_t n, uint64_t h = 1469598103934665603ull) {
+  const uint8_t* b = static_cast<const uint8_t*>(data);
+  for (size_t i = 0; i < n; ++i) h = (h ^ b[i]) * 1099511628211ull;
+  return h;
+}
+
+uint64_t desc_check(const fg_bshuf* d) { return fnv1a(d, offsetof(fg_bshuf, check)) ^ 0x5eedf00dcafe1234ull; }
+
+fg_status check_desc(const fg_bshuf* d) {
+  if (!d) return fail(FG_ERR_INVALID_ARG, "null weight descriptor");
+  if (d->magic != FG_BSHUF_MAGIC || d->version != FG_BSHUF_VERSION || d->check != desc_check(d))
+    return fail(FG_ERR_LAYOUT, "weight descriptor was not produced by fg_preshuffle_b (or was modified)");
+  return FG_OK;
+}
+
+uint64_t sf_image_bytes(int mode, int64_t N, int64_t K) {
+  switch (mode) {
+    case FG_FP8_TENSOR: return 16;
+    case FG_FP8_BLOCK128: return static_cast<uint64_t>(N / 128) * (K / 128) * 4;
+    case FG_MXFP8: return static_cast<uint64_t>(N / 128) * (K / 128) * 512;
+    case FG_MXFP4: return static_cast<uint64_t>(N / 128) * (K / 256) * 2 * 512;
+    default: return 0;
+  }
+}
+
+// ------------------------------------------------------------ dispatch
+
+struct TableRow {
+  int mode;
+  int64_t m_max;  // rows of A up to which the row applies (bucket upper bound)
+  int64_t N, K;
+  int split, sps, stages;
+};
+
+// Exact-shape rows (decode shapes measured on this part); anything else
+// falls through to the heuristic below.
+const TableRow kTable[] = {
+    {FG_FP8_TENSOR, 1, 2048, 7168, 8, 1, 8},   {FG_FP8_TENSOR, 16, 2048, 7168, 8, 1, 8},
+    {FG_FP8_TENSOR, 1, 16384, 7168, 1, 2, 5},  {FG_FP8_TENSOR, 16, 16384, 7168, 1, 2, 5},
+    {FG_FP8_BLOCK128, 1, 2048, 7168, 8, 1, 8}, {FG_FP8_BLOCK128, 16, 2048, 7168, 8, 1, 8},
+    {FG_FP8_BLOCK128, 1, 16384, 7168, 1, 2, 5}, {FG_FP8_BLOCK128, 16, 16384, 7168, 1, 2, 5},
+};
+
+int64_t decode_row_limit() { return 16; }
+
+fg_status make_plan(int mode, int64_t M, int64_t N, int64_t K, int split_k, fg_plan* out) {
+  memset(out, 0, sizeof *out);
+  const int64_t Kb = row_bytes(mode, K);
+  const int64_t KB = Kb / 128;
+  const int64_t tiles_n = N / 128;
+  const int64_t tiles_m = (M + 15) / 16;
+  const bool large = M > decode_row_limit() && large_supported(mode);
+  if (large) {
+    if (split_k > 1) return fail(FG_ERR_INVALID_ARG, "the large-M path takes split_k 0 or 1, got %d", split_k);
+    out->path = 1;
+    out->split_k = 1;
+    out->tile_m = 128;
+    out->tile_n = 256;
+    out->stage_slabs = 1;
+    out->stages = 4;
+    const int64_t tiles = ((M + 127) / 128) * (N / 256 + (N % 256 ? 1 : 0));
+    out->ctas = static_cast<int32_t>(tiles < sm_count() ? tiles : sm_count());
+    snprintf(out->name, sizeof out->name, "fg_large_sm103a_%s_m%lld_n%lld_k%lld_128x256", mode_name(mode),
+             (long long)M, (long long)N, (long long)K);
+    return FG_OK;
+  }
+  int split = split_k, sps = 2, stages = 5;
+  bool from_table = false;
+  for (const TableRow& r : kTable) {
+    if (r.mode == mode && r.N == N && r.K == K && M <= r.m_max && (r.m_max == 1 ? M == 1 : M > 1)) {
+      if (split == 0) split = r.split;
+      sps = r.sps;
+      stages = r.stages;
+      from_table = true;
+      break;
+    }
+  }
+  if (split == 0) {
+    // smallest split in {1,2,4,8} that puts at least ~0.8 of a wave of CTAs on
+    // the SMs, keeping >= 4 slabs per split
+    const int64_t want = (static_cast<int64_t>(sm_count()) * 4) / 5;
+    split = 1;
+    while (split < 8 && tiles_n * tiles_m * split < want && KB / (split * 2) >= 4) split *= 2;
+    if (KB / split < 8) sps = 1, stages = 8;
+  }
+  if (split < 1 || split > 16) return fail(FG_ERR_INVALID_ARG, "split_k=%d outside 1..16", split);
+  if (split > KB)
+    return fail(FG_ERR_SHAPE, "split_k=%d exceeds the %lld 128-byte K slabs of K=%lld", split, (long long)KB,
+                (long long)K);
+  out->path = 0;
+  out->split_k = split;
+  out->tile_m = 16;
+  out->tile_n = 128;
+  out->stage_slabs = sps;
+  out->stages = stages;
+  out->ctas = static_cast<int32_t>(tiles_n * tiles_m * split);
+  out->from_table = from_table ? 1 : 0;
+  snprintf(out->name, sizeof out->name, "fg_decode_sm103a_%s_m%lld_n%lld_k%lld_s%d_%dx%d", mode_name(mode),
+           (long long)M, (long long)N, (long long)K, split, sps, stages);
+  return FG_OK;
+}
+
+// ---------------------------------------------------------- TMA set-up
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    cudaDriverEntryPointQueryResult q;
+    void* p = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
+// Byte-typed 2-D map over A ([rows][row_bytes]) with a box of box_rows x 128
+// bytes in the 128-byte swizzle; rows past the end read as zero.
+fg_status make_tmap(CUtensorMap* map, const void* base, int64_t rows, int64_t rbytes, uint32_t box_rows) {
+  auto fn = encode_fn();
+  if (!fn) return fail(FG_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
+  cuuint64_t dims[2] = {static_cast<cuuint64_t>(rbytes), static_cast<cuuint64_t>(rows)};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(rbytes)};
+  cuuint32_t box[2] = {128, box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return fail(FG_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d)", static_cast<int>(r));
+  return FG_OK;
+}
+
+}  // namespace
+
+int sm_count() {
+  static int count[64] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 148;
+  if (!count[dev]) {
+    int c = 0;
+    if (cudaDeviceGetAttribute(&c, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || c <= 0) c = 148;
+    count[dev] = c;
+  }
+  return count[dev];
+}
+
+}  // namespace fg
+
+using namespace fg;
+
+extern "C" {
+
+int fg_version(void) { return 100; }
+
+const char* fg_status_str(int s) {
+  switch (s) {
+    case FG_OK: return "FG_OK";
+    case FG_ERR_INVALID_ARG: return "FG_ERR_INVALID_ARG";
+    case FG_ERR_SHAPE: return "FG_ERR_SHAPE";
+    case FG_ERR_ALIGN: return "FG_ERR_ALIGN";
+    case FG_ERR_LAYOUT: return "FG_ERR_LAYOUT";
+    case FG_ERR_WORKSPACE: return "FG_ERR_WORKSPACE";
+    case FG_ERR_UNSUPPORTED_ARCH: return "FG_ERR_UNSUPPORTED_ARCH";
+    case FG_ERR_CUDA: return "FG_ERR_CUDA";
+    case FG_ERR_TIMEOUT: return "FG_ERR_TIMEOUT";
+    default: return "FG_ERR_UNKNOWN";
+  }
+}
+
+const char* fg_last_error_message(void) { return g_msg; }
+
+void fg_set_wait_timeout_ns(uint64_t ns) { g_timeout_ns.store(ns ? ns : 1); }
+
+void fg_debug_override_cc(int major, int minor) {
+  g_cc_minor_override.store(minor);
+  g_cc_major_override.store(major);
+}
+
+fg_status fg_preshuffle_b_size(int mode, int64_t N, int64_t K, uint64_t* b_bytes, uint64_t* sf_bytes) {
+  if (!mode_ok(mode)) return fail(FG_ERR_INVALID_ARG, "bad mode %d", mode);
+  if (!b_bytes || !sf_bytes) return fail(FG_ERR_INVALID_ARG, "null output pointer");
+  fg_status s = check_nk(mode, N, K);
+  if (s != FG_OK) return s;
+  *b_bytes = static_cast<uint64_t>(N) * row_bytes(mode, K);
+  *sf_bytes = sf_image_bytes(mode, N, K);
+  return FG_OK;
+}
+
+fg_status fg_preshuffle_b(int mode, const void* B, const void* b_scales, int64_t N, int64_t K, void* b_image,
+                          uint64_t b_image_bytes, void* sf_image, uint64_t sf_image_bytes, fg_bshuf* desc_out,
+                          void* stream) {
+  uint64_t need_b = 0, need_sf = 0;
+  fg_status s = fg_preshuffle_b_size(mode, N, K, &need_b, &need_sf);
+  if (s != FG_OK) return s;
+  if (!B || !b_image || !desc_out) return fail(FG_ERR_INVALID_ARG, "null B, image or descriptor");
+  if (mode == FG_BF16 && b_scales) return fail(FG_ERR_INVALID_ARG, "bf16 weights take no scales");
+  if (mode != FG_BF16 && (!b_scales || !sf_image)) return fail(FG_ERR_INVALID_ARG, "%s needs B scales and a scale image", mode_name(mode));
+  if (!aligned(B, 16) || !aligned(b_image, 16) || (sf_image && !aligned(sf_image, 16)))
+    return fail(FG_ERR_ALIGN, "B and the images must be 16-byte aligned");
+  if (b_scales && !aligned(b_scales, (mode == FG_MXFP8 || mode == FG_MXFP4) ? 1 : 4))
+    return fail(FG_ERR_ALIGN, "fp32 scales must be 4-byte aligned");
+  if (b_image_bytes < need_b || sf_image_bytes < need_sf)
+    return fail(FG_ERR_WORKSPACE, "image buffers too small (need %llu and %llu bytes)", (unsigned long long)need_b,
+                (unsigned long long)need_sf);
+  const uint8_t* b0 = static_cast<const uint8_t*>(B);
+  const uint8_t* i0 = static_cast<const uint8_t*>(b_image);
+  if (b0 < i0 + need_b && i0 < b0 + need_b) return fail(FG_ERR_INVALID_ARG, "B and its image overlap");
+  if ((s = check_arch()) != FG_OK) return s;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  cudaError_t e = launch_relayout_b(b0, static_cast<uint8_t*>(b_image), N, row_bytes(mode, K), false, st);
+  if (e != cudaSuccess) return cuda_fail(e, "weight relayout launch");
+  if (mode == FG_FP8_TENSOR || mode == FG_FP8_BLOCK128) {
+    e = cudaMemcpyAsync(sf_image, b_scales, mode == FG_FP8_TENSOR ? 4 : need_sf, cudaMemcpyDeviceToDevice, st);
+    if (e != cudaSuccess) return cuda_fail(e, "scale copy");
+  } else if (mode == FG_MXFP8 || mode == FG_MXFP4) {
+    e = launch_relayout_sf(mode, static_cast<const uint8_t*>(b_scales), static_cast<uint8_t*>(sf_image), N, K, false,
+                           st);
+    if (e != cudaSuccess) return cuda_fail(e, "scale relayout launch");
+  }
+  fg_bshuf d;
+  memset(&d, 0, sizeof d);
+  d.magic = FG_BSHUF_MAGIC;
+  d.version = FG_BSHUF_VERSION;
+  d.mode = mode;
+  d.tile_rows = 128;
+  d.N = N;
+  d.K = K;
+  d.data = b_image;
+  d.sf = mode == FG_BF16 ? nullptr : sf_image;
+  d.data_bytes = need_b;
+  d.sf_bytes = need_sf;
+  d.check = desc_check(&d);
+  *desc_out = d;
+  return FG_OK;
+}
+
+fg_status fg_unshuffle_b(const fg_bshuf* desc, void* B_out, void* b_scales_out, void* stream) {
+  fg_status s = check_desc(desc);
+  if (s != FG_OK) return s;
+  if (!B_out) return fail(FG_ERR_INVALID_ARG, "null output");
+  if (!aligned(B_out, 16)) return fail(FG_ERR_ALIGN, "B_out must be 16-byte aligned");
+  if ((s = check_arch()) != FG_OK) return s;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  cudaError_t e = launch_relayout_b(static_cast<const uint8_t*>(desc->data), static_cast<uint8_t*>(B_out), desc->N,
+                                    row_bytes(desc->mode, desc->K), true, st);
+  if (e != cudaSuccess) return cuda_fail(e, "inverse relayout launch");
+  if (b_scales_out && desc->sf) {
+    if (desc->mode == FG_FP8_TENSOR || desc->mode == FG_FP8_BLOCK128) {
+      e = cudaMemcpyAsync(b_scales_out, desc->sf, desc->mode == FG_FP8_TENSOR ? 4 : desc->sf_bytes,
+                          cudaMemcpyDeviceToDevice, st);
+    } else {
+      e = launch_relayout_sf(desc->mode, static_cast<const uint8_t*>(desc->sf), static_cast<uint8_t*>(b_scales_out),
+                             desc->N, desc->K, true, st);
+    }
+    if (e != cudaSuccess) return cuda_fail(e, "inverse scale relayout");
+  }
+  return FG_OK;
+}
+
+fg_status fg_gemm_plan(int mode, int64_t M, int64_t N, int64_t K, int split_k, fg_plan* out) {
+  if (!mode_ok(mode)) return fail(FG_ERR_INVALID_ARG, "bad mode %d", mode);
+  if (!out) return fail(FG_ERR_INVALID_ARG, "null plan");
+  if (M < 0) return fail(FG_ERR_SHAPE, "M=%lld is negative", (long long)M);
+  if (split_k < 0 || split_k > 16) return fail(FG_ERR_INVALID_ARG, "split_k=%d outside 0..16", split_k);
+  fg_status s = check_nk(mode, N, K);
+  if (s != FG_OK) return s;
+  return make_plan(mode, M > 0 ? M : 1, N, K, split_k, out);
+}
+
+fg_status fg_gemm_workspace_size(int mode, int64_t M, int64_t N, int64_t K, int split_k, uint64_t* bytes) {
+  if (!bytes) return fail(FG_ERR_INVALID_ARG, "null output");
+  fg_plan plan;
+  fg_status s = fg_gemm_plan(mode, M, N, K, split_k, &plan);
+  if (s != FG_OK) return s;
+  *bytes = plan.split_k > 1 ? static_cast<uint64_t>(plan.split_k) * M * N * 4 : 0;
+  return FG_OK;
+}
+
+fg_status fg_gemm(const void* A, const void* a_scales, int64_t M, const fg_bshuf* b, int mode, int split_k, void* Y,
+                  void* workspace, uint64_t workspace_bytes, uint32_t flags, void* stream) {
+  fg_status s = check_desc(b);
+  if (s != FG_OK) return s;
+  if (!mode_ok(mode)) return fail(FG_ERR_INVALID_ARG, "bad mode %d", mode);
+  if (b->mode != mode)
+    return fail(FG_ERR_LAYOUT, "weight was preshuffled for %s, call asks for %s", mode_name(b->mode), mode_name(mode));
+  if (flags & ~(FG_FLAG_DEFER_REDUCE | FG_FLAG_DEBUG_STALL)) return fail(FG_ERR_INVALID_ARG, "unknown flags 0x%x", flags);
+  if (M < 0) return fail(FG_ERR_SHAPE, "M=%lld is negative", (long long)M);
+  if (M > (int64_t(1) << 24)) return fail(FG_ERR_SHAPE, "M=%lld too large", (long long)M);
+  if (split_k < 0 || split_k > 16) return fail(FG_ERR_INVALID_ARG, "split_k=%d outside 0..16", split_k);
+  const int64_t N = b->N, K = b->K;
+  if ((s = check_nk(mode, N, K)) != FG_OK) return s;
+  if (M == 0) return FG_OK;
+  if (!A || !Y) return fail(FG_ERR_INVALID_ARG, "null A or Y");
+  if (mode != FG_BF16 && !a_scales) return fail(FG_ERR_INVALID_ARG, "%s needs A scales", mode_name(mode));
+  if (!aligned(A, 16) || !aligned(Y, 16)) return fail(FG_ERR_ALIGN, "A and Y must be 16-byte aligned");
+  if ((mode == FG_FP8_TENSOR || mode == FG_FP8_BLOCK128) && !aligned(a_scales, 4))
+    return fail(FG_ERR_ALIGN, "fp32 A scales must be 4-byte aligned");
+  fg_plan plan;
+  if ((s = make_plan(mode, M, N, K, split_k, &plan)) != FG_OK) return s;
+  const int split = plan.split_k;
+  const bool defer = (flags & FG_FLAG_DEFER_REDUCE) != 0;
+  if (split > 1) {
+    const uint64_t need = static_cast<uint64_t>(split) * M * N * 4;
+    if (!workspace || workspace_bytes < need)
+      return fail(FG_ERR_WORKSPACE, "split_k=%d needs a %llu-byte fp32 workspace", split, (unsigned long long)need);
+    if (!aligned(workspace, 16)) return fail(FG_ERR_ALIGN, "workspace must be 16-byte aligned");
+  } else if (defer) {
+    return fail(FG_ERR_INVALID_ARG, "FG_FLAG_DEFER_REDUCE needs split_k > 1");
+  }
+  if ((s = check_arch()) != FG_OK) return s;
+  uint32_t* err = dev_error_ptr();
+  if (!err) return fail(FG_ERR_CUDA, "device error word unavailable");
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const int64_t rb = row_bytes(mode, K);
+  CUtensorMap tmap;
+  cudaError_t e;
+  if (plan.path == 1) {
+    if ((s = make_tmap(&tmap, A, M, rb, 128)) != FG_OK) return s;
+    LargeParams p;
+    memset(&p, 0, sizeof p);
+    p.b_img = static_cast<const uint8_t*>(b->data);
+    p.b_sf = static_cast<const uint8_t*>(b->sf);
+    p.b_s = static_cast<const float*>(b->sf);
+    p.a_scales = a_scales;
+    p.y = static_cast<__nv_bfloat16*>(Y);
+    p.err = err;
+    p.timeout_ns = g_timeout_ns.load();
+    p.M = static_cast<int>(M);
+    p.N = static_cast<int>(N);
+    p.K = static_cast<int>(K);
+    p.KB = static_cast<int>(rb / 128);
+    p.tiles_m = static_cast<int>((M + 127) / 128);
+    p.tiles_n = static_cast<int>(N / 256 + (N % 256 ? 1 : 0));
+    p.debug_stall = (flags & FG_FLAG_DEBUG_STALL) ? 1 : 0;
+    e = launch_large(mode, tmap, p, plan.ctas, st);
+    if (e != cudaSuccess) return cuda_fail(e, "large-M kernel launch");
+    return FG_OK;
+  }
+  if ((s = make_tmap(&tmap, A, M, rb, 16)) != FG_OK) return s;
+  DecodeParams p;
+  memset(&p, 0, sizeof p);
+  p.b_img = static_cast<const uint8_t*>(b->data);
+  p.b_sf = static_cast<const uint8_t*>(b->sf);
+  p.b_s = static_cast<const float*>(b->sf);
+  p.a_scales = a_scales;
+  p.ws = static_cast<float*>(workspace);
+  p.y = static_cast<__nv_bfloat16*>(Y);
+  p.err = err;
+  p.timeout_ns = g_timeout_ns.load();
+  p.M = static_cast<int>(M);
+  p.N = static_cast<int>(N);
+  p.K = static_cast<int>(K);
+  p.KB = static_cast<int>(rb / 128);
+  p.split = split;
+  p.debug_stall = (flags & FG_FLAG_DEBUG_STALL) ? 1 : 0;
+  DecodeConfig cfg{mode, plan.stage_slabs, plan.stages};
+  if (!decode_config_supported(cfg)) return fail(FG_ERR_INVALID_ARG, "no kernel for config %s", plan.name);
+  dim3 grid(static_cast<unsigned>(N / 128), static_cast<unsigned>(split), static_cast<unsigned>((M + 15) / 16));
+  if (grid.z > 65535) return fail(FG_ERR_SHAPE, "M=%lld too large for the decode path", (long long)M);
+  e = launch_decode(cfg, tmap, p, grid, st);
+  if (e != cudaSuccess) return cuda_fail(e, "decode kernel launch");
+  if (split > 1 && !defer) {
+    const float* as = mode == FG_FP8_TENSOR ? static_cast<const float*>(a_scales) : nullptr;
+    const float* bs = mode == FG_FP8_TENSOR ? static_cast<const float*>(b->sf) : nullptr;
+    e = launch_reduce(p.ws, split, M, N, as, bs, p.y, st);
+    if (e != cudaSuccess) return cuda_fail(e, "split-K reduce launch");
+  }
+  return FG_OK;
+}
+
+fg_status fg_gemm_splitk_reduce(const float* ws, int split_k, int64_t M, int64_t N, const float* a_s,
+                                const float* b_s, void* Y, void* stream) {
+  if (!ws || !Y) return fail(FG_ERR_INVALID_ARG, "null workspace or Y");
+  if ((a_s == nullptr) != (b_s == nullptr)) return fail(FG_ERR_INVALID_ARG, "pass both scales or neither");
+  if (split_k < 1 || split_k > 16) return fail(FG_ERR_SHAPE, "split_k=%d outside 1..16", split_k);
+  if (M < 0 || N < 0 || N % 8) return fail(FG_ERR_SHAPE, "need M >= 0 and N a multiple of 8");
+  if (!aligned(ws, 16) || !aligned(Y, 16)) return fail(FG_ERR_ALIGN, "workspace and Y must be 16-byte aligned");
+  if ((a_s && !aligned(a_s, 4)) || (b_s && !aligned(b_s, 4))) return fail(FG_ERR_ALIGN, "scales must be 4-byte aligned");
+  if (M == 0) return FG_OK;
+  fg_status s = check_arch();
+  if (s != FG_OK) return s;
+  cudaError_t e = launch_reduce(ws, split_k, M, N, a_s, b_s, static_cast<__nv_bfloat16*>(Y), static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "reduce launch");
+  return FG_OK;
+}
+
+fg_status fg_get_error(void) {
+  cudaError_t e = cudaDeviceSynchronize();
+  if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceSynchronize");
+  uint32_t* p = dev_error_ptr();
+  if (!p) return fail(FG_ERR_CUDA, "device error word unavailable");
+  uint32_t v = 0;
+  if ((e = cudaMemcpy(&v, p, 4, cudaMemcpyDeviceToHost)) != cudaSuccess) return cuda_fail(e, "error word read");
+  const uint32_t zero = 0;
+  if ((e = cudaMemcpy(p, &zero, 4, cudaMemcpyHostToDevice)) != cudaSuccess) return cuda_fail(e, "error word reset");
+  if (v == 0) return FG_OK;
+  fail(static_cast<fg_status>(v & 0xff), "kernel error word 0x%x (wait site %u)", v, v >> 8);
+  return static_cast<fg_status>(v & 0xff);
+}
+
+}  // extern "C"

@@ -1,0 +1,377 @@
+// Split-K decode GEMM for small M (aiter PR "FlyDSL split-K preshuffle
+// decode GEMM for small-M shapes (FP8 + MX, gfx950/gfx942)", Summary and
+// What's included), written for sm_103a tensor cores.
+//
+// Orientation ("swap AB"): the weight B is the MMA's M operand (128 rows of
+// N per CTA), the <= 16 token rows of A are the MMA's N operand, so one
+// tcgen05.mma is 128 x 16 x (32 bytes of K) and the fp32 accumulator lives
+// in 16 TMEM columns.  CTA (nt, s, mt) covers weight rows [128 nt, +128),
+// token rows [16 mt, +16) and split s of the K slabs.
+//
+// Warp roles (192 threads):
+//   warp 0    producer: one bulk copy per stage for the contiguous weight
+//             slabs of the preshuffled image, one TMA tensor load per slab
+//             for the token tile (rows beyond M are zero-filled), and for MX
+//             the weight scale atoms (bulk) and token scale atoms (built by
+//             the warp's 32 lanes from the caller's E8M0 bytes);
+//   warp 1    allocates TMEM; lane 0 issues tcgen05.cp (MX scale factors)
+//             and tcgen05.mma, and commits stage releases;
+//   warps 2-5 epilogue: TMEM -> registers -> fp32 partials (split > 1) or
+//             scaled bf16 Y (split == 1).  For FP8_BLOCK128 they also run
+//             the per-128-K promotion: each K slab (one 128-K scale block)
+//             is multiplied into its own TMEM partial, which they read and
+//             fold into fp32 registers as acc += a_s[m][kb] * b_s[nb][kb] *
+//             partial (the software-dequant path the page describes for
+//             gfx942: one plain MMA pass per 128-K scale block).
+//
+// MX scale factors: the block-scaled MMA reads, for row i of an operand, the
+// byte selected by the instruction's scale-factor id in TMEM lane i, column
+// (base + i/32).  tcgen05.cp.32x128b.warpx4 copies a 32-row x 16-byte
+// shared-memory atom into four TMEM columns of every 32-lane quarter, which
+// gives exactly that layout for atoms whose byte 16*(i%32) + 4*(i/32) + j
+// holds row i's scale for the j-th 32-K block.  For the 16 token rows only
+// lanes 0-15 of column 0 are read, so token atoms are laid out 256 bytes
+// apart and overlap (rows 16-31 of one atom are rows 0-15 of the next).
+#include <cuda_bf16.h>
+
+#include <cstdio>
+
+#include "fg_internal.cuh"
+#include "fg_ptx.cuh"
+
+namespace fg {
+
+namespace {
+
+constexpr int kThreads = 192;
+constexpr int kSlabBytes = 16384;   // 128 rows x 128 bytes
+constexpr int kTokSlabBytes = 2048; // 16 rows x 128 bytes
+constexpr int kTokRows = 16;
+
+template <int MODE, int SPS, int STAGES>
+struct DCfg {
+  static constexpr int APS = MODE == kMXFP4 ? 2 : (MODE == kMXFP8 ? 1 : 0);
+  static constexpr int B_BYTES = SPS * kSlabBytes;
+  static constexpr int A_BYTES = SPS * kTokSlabBytes;
+  static constexpr int SFW_BYTES = SPS * APS * 512;
+  static constexpr int SFT_BYTES = APS ? SPS * APS * 256 + 256 : 0;
+  static constexpr int STAGE_RAW = B_BYTES + A_BYTES + SFW_BYTES + SFT_BYTES;
+  static constexpr int STAGE_BYTES = (STAGE_RAW + 1023) / 1024 * 1024;
+  static constexpr int NBUF = 8;  // blockscale TMEM partial buffers
+  static constexpr int SF_COLS = SPS * APS * 4;  // TMEM columns per operand per stage
+  static constexpr int TMEM_NEED = MODE == kBlock ? NBUF * 16 : 32 + STAGES * 2 * SF_COLS;
+  static constexpr int TMEM_COLS =
+      TMEM_NEED <= 32 ? 32 : (TMEM_NEED <= 64 ? 64 : (TMEM_NEED <= 128 ? 128 : (TMEM_NEED <= 256 ? 256 : 512)));
+  static constexpr int SMEM = STAGES * STAGE_BYTES + 1024;
+  static_assert(TMEM_NEED <= 512, "TMEM budget");
+  static_assert(SMEM <= 232448, "shared memory budget");
+};
+
+__device__ __forceinline__ uint32_t mx_idesc(int mode, int sfid) {
+  return mode == kMXFP4 ? idesc_mx(128, kTokRows, 1u, sfid, sfid) : idesc_mx(128, kTokRows, 0u, sfid, sfid);
+}
+
+template <int MODE, int SPS, int STAGES>
+__global__ void __launch_bounds__(kThreads, 1)
+    decode_kernel(const __grid_constant__ CUtensorMap tmap_a, const DecodeParams p) {
+  using C = DCfg<MODE, SPS, STAGES>;
+  extern __shared__ uint8_t dsmem[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(dsmem) + 1023) & ~uintptr_t(1023));
+
+  __shared__ __align__(8) uint64_t full_bar[STAGES];
+  __shared__ __align__(8) uint64_t empty_bar[STAGES];
+  __shared__ __align__(8) uint64_t pfull_bar[C::NBUF];
+  __shared__ __align__(8) uint64_t pempty_bar[C::NBUF];
+  __shared__ __align__(8) uint64_t acc_bar, stall_bar, drain_bar;
+  __shared__ uint32_t tmem_base_sh;
+  __shared__ int abort_sh, issued_sh, consumed_sh, mma_any_sh;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int nt = blockIdx.x, split = blockIdx.y, mt = blockIdx.z;
+  const int q = p.KB / p.split, r = p.KB % p.split;
+  const int u0 = split * q + min(split, r);
+  const int nslab = q + (split < r ? 1 : 0);
+  const int niter = (nslab + SPS - 1) / SPS;
+  const uint64_t T = p.timeout_ns;
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < STAGES; ++i) {
+      mbar_init(&full_bar[i], C::APS ? 2 : 1);
+      mbar_init(&empty_bar[i], 1);
+    }
+    for (int i = 0; i < C::NBUF; ++i) {
+      mbar_init(&pfull_bar[i], 1);
+      mbar_init(&pempty_bar[i], 4);
+    }
+    mbar_init(&acc_bar, 1);
+    mbar_init(&stall_bar, 1);
+    mbar_init(&drain_bar, 1);
+    abort_sh = 0;
+    issued_sh = 0;
+    consumed_sh = 0;
+    mma_any_sh = 0;
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(&tmem_base_sh, C::TMEM_COLS);
+    tmem_relinquish();
+  }
+  if (warp == 0 && lane == 0) prefetch_tmap(&tmap_a);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = tmem_base_sh;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    int it = 0;
+    for (; it < niter; ++it) {
+      const int slot = it % STAGES;
+      const uint32_t ph = (it / STAGES) & 1;
+      const bool ok = mbar_wait(&empty_bar[slot], ph ^ 1u, T, p.err, 1);
+      if (!__all_sync(0xffffffffu, ok)) {
+        if (lane == 0) abort_sh = 1;
+        break;
+      }
+      const int ub = it * SPS;
+      const int nsl = min(SPS, nslab - ub);
+      uint8_t* st = smem + slot * C::STAGE_BYTES;
+      if (lane == 0) {
+        const uint32_t bytes = nsl * (kSlabBytes + kTokSlabBytes + C::APS * 512);
+        mbar_arrive_expect_tx(&full_bar[slot], bytes);
+        bulk_g2s(st, p.b_img + (static_cast<size_t>(nt) * p.KB + u0 + ub) * kSlabBytes, nsl * kSlabBytes,
+                 &full_bar[slot]);
+        for (int v = 0; v < nsl; ++v)
+          tma_load_2d(st + C::B_BYTES + v * kTokSlabBytes, &tmap_a, (u0 + ub + v) * 128, mt * kTokRows,
+                      &full_bar[slot]);
+        if (C::APS)
+          bulk_g2s(st + C::B_BYTES + C::A_BYTES,
+                   p.b_sf + (static_cast<size_t>(nt) * p.KB + u0 + ub) * C::APS * 512, nsl * C::APS * 512,
+                   &full_bar[slot]);
+      }
+      if (C::APS) {
+        // token scale atoms: atom t, row m -> 4 bytes (the atom's four 32-K blocks)
+        const uint8_t* asf = static_cast<const uint8_t*>(p.a_scales);
+        uint8_t* sft = st + C::B_BYTES + C::A_BYTES + C::SFW_BYTES;
+        const int natoms = nsl * C::APS;
+        for (int idx = lane; idx < natoms * kTokRows; idx += 32) {
+          const int t = idx / kTokRows, m = idx % kTokRows;
+          const int row = mt * kTokRows + m;
+          uint32_t w = 0x7F7F7F7Fu;  // 2^0 for padded rows (their values are zero)
+          if (row < p.M) {
+            const int q32 = ((u0 + ub) * C::APS + t) * 4;  // first 32-K block of the atom
+            if (MODE == kMXFP4) {
+              const uint8_t* src = asf + static_cast<size_t>(row) * (p.K / 32) + q32;
+              w = static_cast<uint32_t>(src[0]) | (static_cast<uint32_t>(src[1]) << 8) |
+                  (static_cast<uint32_t>(src[2]) << 16) | (static_cast<uint32_t>(src[3]) << 24);
+            } else {
+              const uint32_t c = asf[static_cast<size_t>(row) * (p.K / 128) + (q32 >> 2)];
+              w = c * 0x01010101u;
+            }
+          }
+          *reinterpret_cast<uint32_t*>(sft + t * 256 + m * 16) = w;
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&full_bar[slot]);
+      }
+    }
+    if (lane == 0) issued_sh = it;
+  } else if (warp == 1) {
+    // ---------------------------------------------------------- MMA issuer
+    if (lane == 0) {
+      bool ok = true;
+      if (p.debug_stall) ok = mbar_wait(&stall_bar, 0, T, p.err, 2);
+      int it = 0, slab_ctr = 0;
+      for (; ok && it < niter; ++it) {
+        const int slot = it % STAGES;
+        const uint32_t ph = (it / STAGES) & 1;
+        if (!mbar_wait(&full_bar[slot], ph, T, p.err, 3)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        mma_any_sh = 1;
+        const int nsl = min(SPS, nslab - it * SPS);
+        uint8_t* st = smem + slot * C::STAGE_BYTES;
+        const uint32_t sfw_col = 32 + slot * 2 * C::SF_COLS;
+        const uint32_t sft_col = sfw_col + C::SF_COLS;
+        if (C::APS) {
+          for (int t = 0; t < nsl * C::APS; ++t) {
+            tc_cp_32x128b_warpx4(tmem + sfw_col + 4 * t, sdesc_plain_rows16(smem_u32(st + C::B_BYTES + C::A_BYTES + 512 * t)));
+            tc_cp_32x128b_warpx4(tmem + sft_col + 4 * t,
+                                 sdesc_plain_rows16(smem_u32(st + C::B_BYTES + C::A_BYTES + C::SFW_BYTES + 256 * t)));
+          }
+        }
+        for (int v = 0; v < nsl; ++v) {
+          uint32_t d = tmem;
+          int pb = 0;
+          if (MODE == kBlock) {
+            pb = slab_ctr % C::NBUF;
+            if (!mbar_wait(&pempty_bar[pb], ((slab_ctr / C::NBUF) & 1) ^ 1u, T, p.err, 4)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            d = tmem + pb * 16;
+          }
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            const uint64_t adesc = sdesc_sw128(smem_u32(st + v * kSlabBytes + j * 32));
+            const uint64_t bdesc = sdesc_sw128(smem_u32(st + C::B_BYTES + v * kTokSlabBytes + j * 32));
+            const uint32_t acc = (MODE == kBlock) ? (j > 0) : ((it | v | j) != 0);
+            if (MODE == kBF16) {
+              mma_f16(d, adesc, bdesc, idesc_bf16(128, kTokRows), acc);
+            } else if (MODE == kTensor || MODE == kBlock) {
+              mma_f8f6f4(d, adesc, bdesc, idesc_e4m3(128, kTokRows), acc);
+            } else if (MODE == kMXFP8) {
+              mma_mxf8f6f4(d, adesc, bdesc, mx_idesc(MODE, j), tmem + sfw_col + 4 * v, tmem + sft_col + 4 * v, acc);
+            } else {
+              const int t = v * 2 + (j >> 1);
+              mma_mxf4(d, adesc, bdesc, mx_idesc(MODE, 2 * (j & 1)), tmem + sfw_col + 4 * t, tmem + sft_col + 4 * t,
+                       acc);
+            }
+          }
+          if (MODE == kBlock) {
+            tc_commit(&pfull_bar[pb]);
+            ++slab_ctr;
+          }
+        }
+        if (!ok) {
+          ++it;  // this stage's fill was consumed
+          break;
+        }
+        tc_commit(&empty_bar[slot]);
+      }
+      consumed_sh = it;
+      if (ok && MODE != kBlock) tc_commit(&acc_bar);
+      if (!ok) abort_sh = 1;
+      // every MMA and every commit this thread issued has landed before the
+      // CTA can release TMEM or its barriers
+      if (mma_any_sh) {
+        tc_commit(&drain_bar);
+        mbar_wait(&drain_bar, 0, T, p.err, 7);
+      }
+    }
+  } else {
+    // ------------------------------------------------------------ epilogue
+    const int qd = warp & 3;
+    const int nrow = nt * 128 + qd * 32 + lane;
+    const uint32_t trow = tmem + (static_cast<uint32_t>(qd * 32) << 16);
+    float acc[kTokRows];
+#pragma unroll
+    for (int m = 0; m < kTokRows; ++m) acc[m] = 0.f;
+    bool ok = true;
+    if (MODE == kBlock) {
+      const float* a_s = static_cast<const float*>(p.a_scales);
+      const int KS = p.K / 128;
+      for (int i = 0; i < nslab; ++i) {
+        const int pb = i % C::NBUF;
+        const bool w = mbar_wait(&pfull_bar[pb], (i / C::NBUF) & 1, T, p.err, 5);
+        if (!__all_sync(0xffffffffu, w)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        uint32_t v[16];
+        tmem_ld16(trow + pb * 16, v);
+        tmem_wait_ld();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&pempty_bar[pb]);
+        const int kb = u0 + i;
+        const float bsc = __ldg(p.b_s + static_cast<size_t>(nt) * KS + kb);
+#pragma unroll
+        for (int m = 0; m < kTokRows; ++m) {
+          const int row = mt * kTokRows + m;
+          if (row < p.M) acc[m] = fmaf(__ldg(a_s + static_cast<size_t>(row) * KS + kb) * bsc, __uint_as_float(v[m]), acc[m]);
+        }
+      }
+    } else {
+      const bool w = mbar_wait(&acc_bar, 0, T, p.err, 6);
+      if (!__all_sync(0xffffffffu, w)) {
+        ok = false;
+      } else {
+        tc_fence_after();
+        uint32_t v[16];
+        tmem_ld16(trow, v);
+        tmem_wait_ld();
+#pragma unroll
+        for (int m = 0; m < kTokRows; ++m) acc[m] = __uint_as_float(v[m]);
+      }
+    }
+    if (!ok) {
+      if (lane == 0) abort_sh = 1;
+    } else if (p.split > 1) {
+#pragma unroll
+      for (int m = 0; m < kTokRows; ++m) {
+        const int row = mt * kTokRows + m;
+        if (row < p.M) p.ws[(static_cast<size_t>(split) * p.M + row) * p.N + nrow] = acc[m];
+      }
+    } else {
+      float scale = 1.f;
+      if (MODE == kTensor) scale = __ldg(static_cast<const float*>(p.a_scales)) * __ldg(p.b_s);
+#pragma unroll
+      for (int m = 0; m < kTokRows; ++m) {
+        const int row = mt * kTokRows + m;
+        if (row < p.M) p.y[static_cast<size_t>(row) * p.N + nrow] = __float2bfloat16_rn(acc[m] * scale);
+      }
+    }
+  }
+
+  // ------------------------------------------------------------- teardown
+  tc_fence_before();
+  __syncthreads();
+  if (abort_sh) {
+    // Let every copy this CTA started land before its shared memory goes
+    // away, and every MMA it issued finish before TMEM is released.
+    if (threadIdx.x == 0) {
+      for (int it = consumed_sh; it < issued_sh; ++it)
+        mbar_wait(&full_bar[it % STAGES], (it / STAGES) & 1, T, nullptr, 0);
+    }
+  }
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 1) tmem_dealloc(tmem, C::TMEM_COLS);
+}
+
+template <int MODE, int SPS, int STAGES>
+cudaError_t launch_one(const CUtensorMap& tmap_a, const DecodeParams& p, dim3 grid, cudaStream_t stream) {
+  using C = DCfg<MODE, SPS, STAGES>;
+  static bool attr_set = false;  // per process; the attribute applies to every device
+  if (!attr_set) {
+    cudaError_t e = cudaFuncSetAttribute(decode_kernel<MODE, SPS, STAGES>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+    if (e != cudaSuccess) return e;
+    attr_set = true;
+  }
+  decode_kernel<MODE, SPS, STAGES><<<grid, kThreads, C::SMEM, stream>>>(tmap_a, p);
+  return cudaGetLastError();
+}
+
+// Instantiated configurations: (slabs per stage, stages).
+#define FG_DECODE_CONFIGS(X, MODE) \
+  X(MODE, 1, 8)                    \
+  X(MODE, 2, 5)
+
+}  // namespace
+
+bool decode_config_supported(const DecodeConfig& c) {
+  if (c.mode < kBF16 || c.mode > kMXFP4) return false;
+  return (c.sps == 1 && c.stages == 8) || (c.sps == 2 && c.stages == 5);
+}
+
+cudaError_t launch_decode(const DecodeConfig& c, const CUtensorMap& tmap_a, const DecodeParams& p, dim3 grid,
+                          cudaStream_t stream) {
+#define FG_TRY(MODE_, SPS_, ST_) \
+  if (c.mode == MODE_ && c.sps == SPS_ && c.stages == ST_) return launch_one<MODE_, SPS_, ST_>(tmap_a, p, grid, stream);
+  FG_DECODE_CONFIGS(FG_TRY, kBF16)
+  FG_DECODE_CONFIGS(FG_TRY, kTensor)
+  FG_DECODE_CONFIGS(FG_TRY, kBlock)
+  FG_DECODE_CONFIGS(FG_TRY, kMXFP8)
+  FG_DECODE_CONFIGS(FG_TRY, kMXFP4)
+#undef FG_TRY
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace fg

@@ -1,0 +1,72 @@
+// Internal declarations shared by the library's translation units (host side
+// launchers and the parameter blocks the kernels receive).
+#pragma once
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+namespace fg {
+
+enum Mode : int { kBF16 = 0, kTensor = 1, kBlock = 2, kMXFP8 = 3, kMXFP4 = 4 };
+
+inline int elem_bits(int mode) { return mode == kBF16 ? 16 : (mode == kMXFP4 ? 4 : 8); }
+inline int64_t row_bytes(int mode, int64_t K) { return K * elem_bits(mode) / 8; }
+// 512-byte scale-factor atoms per 128-byte K slab of the weight image.
+inline int sf_atoms_per_slab(int mode) { return mode == kMXFP4 ? 2 : (mode == kMXFP8 ? 1 : 0); }
+
+// Parameters of the split-K decode kernel (weights on the MMA M side,
+// tokens on the N side, 16 tokens per CTA tile).
+struct DecodeParams {
+  const uint8_t* b_img;    // weight image
+  const uint8_t* b_sf;     // MX: weight scale image (atoms)
+  const float* b_s;        // FP8_TENSOR: scalar; FP8_BLOCK128: [N/128][K/128]
+  const void* a_scales;    // FP8_TENSOR: fp32 scalar; BLOCK128: fp32 [M][K/128]; MX: E8M0 [M][K/blk]
+  float* ws;               // [split][M][N] fp32 partials (split > 1)
+  __nv_bfloat16* y;        // [M][N] (split == 1)
+  uint32_t* err;           // device error word
+  uint64_t timeout_ns;     // limit of every wait
+  int M, N, K;
+  int KB;                  // 128-byte slabs per row
+  int split;
+  int debug_stall;
+};
+
+struct DecodeConfig {
+  int mode;
+  int sps;     // slabs per stage
+  int stages;  // pipeline depth
+};
+
+// Parameters of the large-M kernel (A on the MMA M side, 128 x 256 tiles).
+struct LargeParams {
+  const uint8_t* b_img;
+  const uint8_t* b_sf;     // MX weight scale image
+  const float* b_s;        // FP8_TENSOR scalar
+  const void* a_scales;    // FP8_TENSOR scalar / MX E8M0 [M][K/blk]
+  __nv_bfloat16* y;
+  uint32_t* err;
+  uint64_t timeout_ns;
+  int M, N, K;
+  int KB;
+  int tiles_m, tiles_n;
+  int debug_stall;
+};
+
+bool decode_config_supported(const DecodeConfig& c);
+cudaError_t launch_decode(const DecodeConfig& cfg, const CUtensorMap& tmap_a, const DecodeParams& p, dim3 grid,
+                          cudaStream_t stream);
+
+bool large_supported(int mode);
+cudaError_t launch_large(int mode, const CUtensorMap& tmap_a, const LargeParams& p, int ctas, cudaStream_t stream);
+
+cudaError_t launch_relayout_b(const uint8_t* src, uint8_t* dst, int64_t N, int64_t Kb, bool inverse,
+                              cudaStream_t stream);
+cudaError_t launch_relayout_sf(int mode, const uint8_t* src, uint8_t* dst, int64_t N, int64_t K, bool inverse,
+                               cudaStream_t stream);
+cudaError_t launch_reduce(const float* ws, int split, int64_t M, int64_t N, const float* a_s, const float* b_s,
+                          __nv_bfloat16* y, cudaStream_t stream);
+
+int sm_count();
+
+}  // namespace fg

@@ -1,0 +1,135 @@
+// HBM-bound helper kernels: the one-time weight relayout (and its inverse),
+// the scale-factor relayout for MX weights, and the split-K reduce.
+//
+// The weight relayout is the preshuffle step of the aiter PR "FlyDSL split-K
+// preshuffle decode GEMM for small-M shapes (FP8 + MX, gfx950/gfx942)"
+// (Copilot file table: the weight/scale preshuffle helpers).  The pages do
+// not give a layout; this one makes each 128-row x 128-byte K slab the exact
+// shared-memory image of a 128-byte-swizzled K-major tensor-core operand.
+//
+// The reduce is that PR's second pass ("fp32 split-K reduction kernel
+// (downcast once at final store)"): sum the fp32 partials in split order,
+// apply the per-tensor scale, round to bf16 once.
+#include <cuda_bf16.h>
+
+#include "fg_internal.cuh"
+
+namespace fg {
+
+namespace {
+
+int grid_for(int64_t work, int threads) {
+  int64_t blocks = (work + threads - 1) / threads;
+  const int64_t cap = static_cast<int64_t>(sm_count()) * 16;
+  if (blocks > cap) blocks = cap;
+  return static_cast<int>(blocks < 1 ? 1 : blocks);
+}
+
+// One thread per 16-byte chunk.  Chunk c (0..7) of row r in slab (nb, kb)
+// goes to chunk (c ^ (r % 8)) of image row r of slab nb*KB + kb.
+__global__ void relayout_b_kernel(const uint4* __restrict__ src, uint4* __restrict__ dst, int64_t N, int64_t Kb,
+                                  int inverse) {
+  const int64_t chunks_per_row = Kb >> 4;
+  const int64_t KB = Kb >> 7;
+  const int64_t total = N * chunks_per_row;
+  for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < total;
+       i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const int64_t n = i / chunks_per_row, cc = i - n * chunks_per_row;
+    const int64_t kb = cc >> 3, c = cc & 7, nb = n >> 7, r = n & 127;
+    const int64_t img = (((nb * KB + kb) << 7) + r) * 8 + (c ^ (r & 7));
+    if (!inverse)
+      dst[img] = __ldg(src + i);
+    else
+      dst[i] = __ldg(src + img);
+  }
+}
+
+// MX weight scales [N][K/blk] (E8M0 bytes) <-> atoms of 512 bytes: for each
+// 128-row tile nb, slab u and atom a of the slab, byte 16*(r%32) + 4*(r/32) + j
+// holds the scale of row nb*128 + r for the 32-K block (u*APS + a)*4 + j.
+// mxfp8 scales cover 128 K, so the four 32-K blocks of a slab repeat one.
+__global__ void relayout_sf_kernel(const uint8_t* __restrict__ src, uint8_t* __restrict__ dst, int64_t N, int64_t K,
+                                   int mode, int inverse) {
+  const int aps = mode == kMXFP4 ? 2 : 1;
+  const int64_t KB = mode == kMXFP4 ? K / 256 : K / 128;  // slabs per row
+  const int64_t sf_cols = mode == kMXFP4 ? K / 32 : K / 128;
+  const int64_t total = (N / 128) * KB * aps * 512;
+  for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < total;
+       i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const int64_t atom = i >> 9;
+    const int off = static_cast<int>(i & 511);
+    const int r = (off >> 4) + 32 * ((off & 15) >> 2);
+    const int j = off & 3;
+    const int64_t nb = atom / (KB * aps);
+    const int64_t rem = atom - nb * KB * aps;
+    const int64_t q32 = rem * 4 + j;  // (u*aps + a)*4 + j
+    const int64_t n = nb * 128 + r;
+    const int64_t col = mode == kMXFP4 ? q32 : (q32 >> 2);
+    if (!inverse) {
+      dst[i] = __ldg(src + n * sf_cols + col);
+    } else if (mode == kMXFP4 || j == 0) {
+      dst[n * sf_cols + col] = __ldg(src + i);
+    }
+  }
+}
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+  const __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<const uint32_t*>(&v);
+}
+
+// Y[i] = bf16_rne(scale * sum_s ws[s][i]) over the flattened M*N outputs,
+// eight consecutive outputs per thread (two 16-byte loads per split, one
+// 16-byte store).
+__global__ void reduce_kernel(const float4* __restrict__ ws, int split, int64_t mn8, const float* __restrict__ a_s,
+                              const float* __restrict__ b_s, uint4* __restrict__ y) {
+  const float scale = (a_s != nullptr) ? __ldg(a_s) * __ldg(b_s) : 1.0f;
+  const int64_t mn4 = mn8 * 2;
+  for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < mn8;
+       i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    float4 a = __ldcs(ws + 2 * i), b = __ldcs(ws + 2 * i + 1);
+    for (int s = 1; s < split; ++s) {
+      const float4 c = __ldcs(ws + s * mn4 + 2 * i), d = __ldcs(ws + s * mn4 + 2 * i + 1);
+      a.x += c.x; a.y += c.y; a.z += c.z; a.w += c.w;
+      b.x += d.x; b.y += d.y; b.z += d.z; b.w += d.w;
+    }
+    uint4 o;
+    o.x = pack_bf16x2(a.x * scale, a.y * scale);
+    o.y = pack_bf16x2(a.z * scale, a.w * scale);
+    o.z = pack_bf16x2(b.x * scale, b.y * scale);
+    o.w = pack_bf16x2(b.z * scale, b.w * scale);
+    y[i] = o;
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_relayout_b(const uint8_t* src, uint8_t* dst, int64_t N, int64_t Kb, bool inverse,
+                              cudaStream_t stream) {
+  const int64_t work = N * (Kb / 16);
+  if (work == 0) return cudaSuccess;
+  relayout_b_kernel<<<grid_for(work, 256), 256, 0, stream>>>(reinterpret_cast<const uint4*>(src),
+                                                             reinterpret_cast<uint4*>(dst), N, Kb, inverse ? 1 : 0);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_relayout_sf(int mode, const uint8_t* src, uint8_t* dst, int64_t N, int64_t K, bool inverse,
+                               cudaStream_t stream) {
+  const int aps = mode == kMXFP4 ? 2 : 1;
+  const int64_t KB = mode == kMXFP4 ? K / 256 : K / 128;
+  const int64_t work = (N / 128) * KB * aps * 512;
+  if (work == 0) return cudaSuccess;
+  relayout_sf_kernel<<<grid_for(work, 256), 256, 0, stream>>>(src, dst, N, K, mode, inverse ? 1 : 0);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_reduce(const float* ws, int split, int64_t M, int64_t N, const float* a_s, const float* b_s,
+                          __nv_bfloat16* y, cudaStream_t stream) {
+  const int64_t mn8 = M * N / 8;
+  if (mn8 == 0) return cudaSuccess;
+  reduce_kernel<<<grid_for(mn8, 256), 256, 0, stream>>>(reinterpret_cast<const float4*>(ws), split, mn8, a_s, b_s,
+                                                        reinterpret_cast<uint4*>(y));
+  return cudaGetLastError();
+}
+
+}  // namespace fg

@@ -42,6 +42,8 @@ def lib():
         L.orc_preshuffle_b.restype = ctypes.c_int
         L.orc_unshuffle_b.argtypes = [vp, i64, i64, vp]
         L.orc_unshuffle_b.restype = ctypes.c_int
+        L.orc_sf_image.argtypes = [ctypes.c_int, vp, i64, i64, vp]
+        L.orc_sf_image.restype = ctypes.c_int
         L.orc_round_bf16.argtypes = [vp, i64, vp]
         L.orc_decode_bf16.argtypes = [vp, i64, vp]
         for f in (L.orc_table_e4m3, L.orc_table_e2m1, L.orc_table_e8m0):
@@ -163,6 +165,16 @@ def unshuffle_b(img, N, Kb):
     out = np.empty((N, Kb), np.uint8)
     if lib().orc_unshuffle_b(_ptr(img), N, Kb, _ptr(out)) != 0:
         raise ValueError("bad preshuffle shape")
+    return out
+
+
+def sf_image(mode, sf, N, K):
+    """MX weight-scale image (layout spec), uint8 of N/128 * slabs * atoms * 512 bytes."""
+    sf = _c(sf, np.uint8)
+    atoms, slab_k = (2, 256) if mode == MXFP4 else (1, 128)
+    out = np.zeros((N // 128) * (K // slab_k) * atoms * 512, np.uint8)
+    if lib().orc_sf_image(mode, _ptr(sf), N, K, _ptr(out)) != 0:
+        raise ValueError("bad scale image arguments")
     return out
 
 

@@ -334,3 +334,34 @@ void orc_round_bf16(const double *in, int64_t n, uint16_t *out)
     for (int64_t i = 0; i < n; ++i)
         out[i] = f32_to_bf16_rne((float)in[i]);
 }
+
+/* ------------------------------------------- MX scale image (layout spec) */
+
+/*
+ * The weight scale image of the MX modes.  For each 128-row tile nb, each
+ * 128-byte K slab u and each atom a of the slab (one atom per slab for mxfp8,
+ * two for mxfp4), a 512-byte atom whose byte 16*(r%32) + 4*(r/32) + j holds
+ * the E8M0 scale of row nb*128 + r for the 32-K block (u*atoms + a)*4 + j.
+ * An mxfp8 scale covers 128 K, i.e. the four 32-K blocks of its slab.
+ * sf is [N][K/128] (mxfp8) or [N][K/32] (mxfp4).
+ */
+int orc_sf_image(int mode, const uint8_t *sf, int64_t N, int64_t K, uint8_t *out)
+{
+    if ((mode != ORC_MXFP8 && mode != ORC_MXFP4) || N % 128 != 0)
+        return -1;
+    const int64_t slab_k = mode == ORC_MXFP4 ? 256 : 128;
+    if (K % slab_k != 0)
+        return -1;
+    const int64_t atoms = mode == ORC_MXFP4 ? 2 : 1;
+    const int64_t slabs = K / slab_k;
+    const int64_t cols = mode == ORC_MXFP4 ? K / 32 : K / 128;
+    for (int64_t n = 0; n < N; ++n)
+        for (int64_t q = 0; q < K / 32; ++q) {          /* 32-K block index */
+            const int64_t nb = n / 128, r = n % 128;
+            const int64_t u = q / (4 * atoms), a = (q / 4) % atoms, j = q % 4;
+            const int64_t atom = (nb * slabs + u) * atoms + a;
+            const uint8_t v = mode == ORC_MXFP4 ? sf[n * cols + q] : sf[n * cols + q / 4];
+            out[atom * 512 + 16 * (r % 32) + 4 * (r / 32) + j] = v;
+        }
+    return 0;
+}

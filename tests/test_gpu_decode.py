@@ -1,0 +1,199 @@
+"""Parity of the split-K decode GEMM (all scale modes) with the oracle.
+
+Bounds: fp32 workspace |ws - ref| <= 1e-5 |ref| + 1e-6 rms(ref); bf16 Y
+|y - ref| <= 2e-2 rms(ref) per element; closed forms bit-exact.
+"""
+import numpy as np
+import pytest
+import torch
+
+import inputs
+import mx_gemm_gb300 as fg
+import oracle
+from tests import parity
+from tests.gpu_util import Case, dev, host, y_to_f64
+
+pytestmark = pytest.mark.gpu
+
+MODES = ["bf16", "fp8_tensor", "fp8_block128", "mxfp8", "mxfp4"]
+
+
+def _slabs(mode, K):
+    return {"bf16": K // 64, "mxfp4": K // 256}.get(mode, K // 128)
+
+
+@pytest.mark.parametrize("mode", MODES)
+@pytest.mark.parametrize("M,N,K", [(1, 128, 1536), (3, 384, 1536), (16, 256, 3072), (17, 128, 1536),
+                                   (40, 256, 1024)])
+@pytest.mark.parametrize("S", [1, 2, 4, 8])
+def test_decode_small_shapes(mode, M, N, K, S):
+    if S > _slabs(mode, K):
+        pytest.skip("more splits than K slabs")
+    c = Case(mode, *inputs.operands(mode, M, N, K, 100 + M, 200 + N, 300 + K))
+    ref = c.ref()
+    if S > 1:
+        ws = c.partials(S)
+        parity.assert_ws_close(ws, c.ref_ws(S), f"{mode} ws S={S}")
+    y = y_to_f64(c.gemm(split_k=S))
+    parity.assert_y_close(y, ref, f"{mode} y S={S}")
+
+
+@pytest.mark.parametrize("mode", MODES)
+def test_split_outputs_agree(mode):
+    M, N, K = 4, 256, 2048
+    c = Case(mode, *inputs.operands(mode, M, N, K, 1, 2, 3))
+    y1 = y_to_f64(c.gemm(split_k=1))
+    for S in (2, 4, 8):
+        if S > _slabs(mode, K):
+            continue
+        yS = y_to_f64(c.gemm(split_k=S))
+        parity.assert_y_close(yS, y1, f"{mode} split {S} vs 1")
+
+
+@pytest.mark.parametrize("mode", MODES)
+def test_deferred_reduce_equals_fused_call(mode):
+    M, N, K, S = 16, 256, 2048, 4
+    c = Case(mode, *inputs.operands(mode, M, N, K, 9, 10, 11))
+    ws = torch.empty(S * M * N, dtype=torch.float32, device="cuda")
+    c.gemm(split_k=S, flags=fg.FG_FLAG_DEFER_REDUCE, workspace=ws)
+    y_two = c.reduce(ws, S)
+    y_one = c.gemm(split_k=S)
+    assert torch.equal(y_two.view(torch.int16), y_one.view(torch.int16))
+
+
+ONE = {"bf16": 0x3F80, "fp8_tensor": 0x38, "fp8_block128": 0x38, "mxfp8": 0x38, "mxfp4": 0x2}
+
+
+def _unit_a_scales(mode, M, K):
+    return {"fp8_tensor": np.array([1.0], np.float32),
+            "fp8_block128": np.ones((M, K // 128), np.float32),
+            "mxfp8": np.full((M, K // 128), 127, np.uint8),
+            "mxfp4": np.full((M, K // 32), 127, np.uint8)}.get(mode)
+
+
+@pytest.mark.parametrize("mode", MODES)
+@pytest.mark.parametrize("S", [1, 4])
+def test_identity_is_bit_exact(mode, S):
+    """A = rows of the identity: Y[m, n] = Bd[n, m] exactly (bf16 holds every
+    e4m3/e2m1 value times a power-of-two scale)."""
+    M, N, K = 16, 256, 2048
+    _, B, _, b_s = inputs.operands(mode, 1, N, K, 41, 42, 43)
+    if mode == "fp8_block128":
+        b_s = np.full_like(b_s, 0.5)
+    if mode == "fp8_tensor":
+        b_s = np.array([1.0], np.float32)
+    A = np.zeros((M, K), np.uint16 if mode == "bf16" else np.uint8)
+    for m in range(M):
+        A[m, 37 * m + 5] = ONE[mode]
+    if mode == "mxfp4":
+        A = inputs.pack_e2m1(A)
+    c = Case(mode, A, B, _unit_a_scales(mode, M, K), b_s)
+    ref = c.ref()
+    y = y_to_f64(c.gemm(split_k=S))
+    assert np.array_equal(y, parity.bf16_bits_to_f64(oracle.round_bf16(ref)))
+    assert np.array_equal(parity.bf16_bits_to_f64(oracle.round_bf16(ref)), ref)  # exact in bf16
+
+
+@pytest.mark.parametrize("mode", MODES)
+def test_all_ones_is_exact(mode):
+    M, N, K = 3, 128, 7168 if mode != "bf16" else 4096
+    A = np.full((M, K if mode != "mxfp4" else K // 2),
+                ONE[mode] if mode != "mxfp4" else 0x22, np.uint16 if mode == "bf16" else np.uint8)
+    B = np.full((N, A.shape[1]), A.flat[0], A.dtype)
+    b_s = {"fp8_tensor": np.array([1.0], np.float32), "fp8_block128": np.ones((1, K // 128), np.float32),
+           "mxfp8": np.full((N, K // 128), 127, np.uint8), "mxfp4": np.full((N, K // 32), 127, np.uint8)}.get(mode)
+    c = Case(mode, A, B, _unit_a_scales(mode, M, K), b_s)
+    for S in (1, 4):
+        y = y_to_f64(c.gemm(split_k=S))
+        assert np.all(y == K)
+
+
+# ----------------------------------------------------- full decode shapes
+
+DECODE = [(m, n) for m, n in inputs.DECODE_SHAPES]
+
+
+@pytest.mark.parametrize("mode", ["fp8_tensor", "fp8_block128", "mxfp8", "mxfp4"])
+@pytest.mark.parametrize("M,N", DECODE)
+def test_decode_workload_parity(mode, M, N):
+    """The pages' decode shapes (K=7168) in the dispatch-chosen configuration,
+    every output compared."""
+    K = 7168
+    c = Case(mode, *inputs.operands(mode, M, N, K, 1000 + M, 2000 + N, 3000))
+    plan = fg.gemm_plan(mode, M, N, K)
+    ref = c.ref()
+    S = plan["split_k"]
+    if S > 1:
+        parity.assert_ws_close(c.partials(S), c.ref_ws(S), f"{mode} {M}x{N} ws")
+    y = y_to_f64(c.gemm())
+    parity.assert_y_close(y, ref, f"{mode} {M}x{N}")
+
+
+# -------------------------------------------------------- negative controls
+
+def test_negative_controls_diverge():
+    """Planted mistakes must fail the bounds: a wrong scale, a weight that was
+    not preshuffled, swapped fp4 nibbles."""
+    M, N, K = 4, 256, 2048
+    c = Case("fp8_tensor", *inputs.operands("fp8_tensor", M, N, K, 51, 52, 53))
+    ref = c.ref()
+    y = y_to_f64(fg.gemm(c.dA, c.pb, dev(c.a_s * 2)))
+    assert parity.y_violations(y, ref)[0] > 0
+    raw = Case("fp8_tensor", c.A, c.B, c.a_s, c.b_s)
+    raw.pb.data.copy_(dev(np.ascontiguousarray(c.B).reshape(-1)))   # un-preshuffled bytes
+    assert parity.y_violations(y_to_f64(raw.gemm()), ref)[0] > 0
+    f = Case("mxfp4", *inputs.operands("mxfp4", M, N, K, 54, 55, 56))
+    ref4 = f.ref()
+    swapped = ((f.A & 15) << 4) | (f.A >> 4)
+    y4 = y_to_f64(fg.gemm(dev(swapped.astype(np.uint8)), f.pb, f.da_s))
+    assert parity.y_violations(y4, ref4)[0] > 0
+    assert parity.y_violations(y_to_f64(f.gemm()), ref4)[0] == 0
+
+
+# ------------------------------------------------------------ error paths
+
+def test_error_paths_on_device():
+    M, N, K = 2, 256, 1024
+    c = Case("fp8_tensor", *inputs.operands("fp8_tensor", M, N, K, 61, 62, 63))
+    Y = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
+    with pytest.raises(fg.FgError) as e:
+        fg.gemm(c.dA, c.pb, c.da_s, mode="mxfp8", Y=Y)
+    assert e.value.status == fg.FG_ERR_LAYOUT
+    with pytest.raises(fg.FgError) as e:
+        fg.gemm(c.dA, c.pb, c.da_s, split_k=4, Y=Y, workspace=torch.empty(8, device="cuda"))
+    assert e.value.status == fg.FG_ERR_WORKSPACE
+    buf = torch.zeros(M * K + 16, dtype=torch.uint8, device="cuda")
+    with pytest.raises(fg.FgError) as e:
+        fg.gemm(buf[1:1 + M * K].view(M, K), c.pb, c.da_s, Y=Y)
+    assert e.value.status == fg.FG_ERR_ALIGN
+    with pytest.raises(fg.FgError) as e:
+        fg.gemm(c.dA, c.pb, None, Y=Y)
+    assert e.value.status == fg.FG_ERR_INVALID_ARG
+    fg.debug_override_cc(9, 0)
+    try:
+        with pytest.raises(fg.FgError) as e:
+            fg.gemm(c.dA, c.pb, c.da_s, Y=Y)
+        assert e.value.status == fg.FG_ERR_UNSUPPORTED_ARCH
+    finally:
+        fg.debug_override_cc(-1, 0)
+    # M == 0: no-op
+    fg.gemm(c.dA[:0], c.pb, c.da_s, Y=Y[:0])
+    parity.assert_y_close(y_to_f64(c.gemm()), c.ref(), "after errors")
+
+
+def test_bounded_wait_reports_timeout_and_context_survives():
+    """The MMA issuer waits on a barrier nothing arrives at; every wait runs
+    out after the limit, the kernel cleans up and returns, and the host reads
+    FG_ERR_TIMEOUT.  A normal call afterwards is still correct."""
+    M, N, K = 1, 256, 2048
+    assert fg.get_error() == fg.FG_OK
+    for mode in ("fp8_tensor", "fp8_block128", "mxfp4"):
+        c = Case(mode, *inputs.operands(mode, M, N, K, 71, 72, 73))
+        fg.set_wait_timeout_ns(20_000_000)
+        try:
+            c.gemm(split_k=2, flags=fg.FG_FLAG_DEBUG_STALL)
+            assert fg.get_error() == fg.FG_ERR_TIMEOUT
+        finally:
+            fg.set_wait_timeout_ns(4_000_000_000)
+        assert fg.get_error() == fg.FG_OK
+        parity.assert_y_close(y_to_f64(c.gemm(split_k=2)), c.ref(), f"{mode} after timeout")
