@@ -22,7 +22,10 @@
 //             is multiplied into its own TMEM partial, which they read and
 //             fold into fp32 registers as acc += a_s[m][kb] * b_s[nb][kb] *
 //             partial (the software-dequant path the page describes for
-//             gfx942: one plain MMA pass per 128-K scale block).
+//             gfx942: one plain MMA pass per 128-K scale block).  bf16 uses
+//             the same per-slab partials with a weight of 1: the fold is a
+//             compensated sum, which keeps the fp32 partials of long K
+//             splits within the workspace bound.
 //
 // MX scale factors: the block-scaled MMA reads, for row i of an operand, the
 // byte selected by the instruction's scale-factor id in TMEM lane i, column
@@ -59,7 +62,10 @@ struct DCfg {
   static constexpr int STAGE_BYTES = (STAGE_RAW + 1023) / 1024 * 1024;
   static constexpr int NBUF = 8;  // blockscale TMEM partial buffers
   static constexpr int SF_COLS = SPS * APS * 4;  // TMEM columns per operand per stage
-  static constexpr int TMEM_NEED = MODE == kBlock ? NBUF * 16 : 32 + STAGES * 2 * SF_COLS;
+  // bf16 and fp8-blockscale accumulate each K slab in its own TMEM partial
+  // and fold the partials in registers (compensated), see the epilogue
+  static constexpr bool PROMOTE = MODE == kBlock || MODE == kBF16;
+  static constexpr int TMEM_NEED = PROMOTE ? NBUF * 16 : 32 + STAGES * 2 * SF_COLS;
   static constexpr int TMEM_COLS =
       TMEM_NEED <= 32 ? 32 : (TMEM_NEED <= 64 ? 64 : (TMEM_NEED <= 128 ? 128 : (TMEM_NEED <= 256 ? 256 : 512)));
   static constexpr int SMEM = STAGES * STAGE_BYTES + 1024;
@@ -206,7 +212,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int v = 0; v < nsl; ++v) {
           uint32_t d = tmem;
           int pb = 0;
-          if (MODE == kBlock) {
+          if (C::PROMOTE) {
             pb = slab_ctr % C::NBUF;
             if (!mbar_wait(&pempty_bar[pb], ((slab_ctr / C::NBUF) & 1) ^ 1u, T, p.err, 4)) {
               ok = false;
@@ -219,7 +225,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int j = 0; j < 4; ++j) {
             const uint64_t adesc = sdesc_sw128(smem_u32(st + v * kSlabBytes + j * 32));
             const uint64_t bdesc = sdesc_sw128(smem_u32(st + C::B_BYTES + v * kTokSlabBytes + j * 32));
-            const uint32_t acc = (MODE == kBlock) ? (j > 0) : ((it | v | j) != 0);
+            const uint32_t acc = C::PROMOTE ? (j > 0) : ((it | v | j) != 0);
             if (MODE == kBF16) {
               mma_f16(d, adesc, bdesc, idesc_bf16(128, kTokRows), acc);
             } else if (MODE == kTensor || MODE == kBlock) {
@@ -232,7 +238,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                        acc);
             }
           }
-          if (MODE == kBlock) {
+          if (C::PROMOTE) {
             tc_commit(&pfull_bar[pb]);
             ++slab_ctr;
           }
@@ -244,7 +250,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_commit(&empty_bar[slot]);
       }
       consumed_sh = it;
-      if (ok && MODE != kBlock) tc_commit(&acc_bar);
+      if (ok && !C::PROMOTE) tc_commit(&acc_bar);
       if (!ok) abort_sh = 1;
       // every MMA and every commit this thread issued has landed before the
       // CTA can release TMEM or its barriers
@@ -262,7 +268,15 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
     for (int m = 0; m < kTokRows; ++m) acc[m] = 0.f;
     bool ok = true;
-    if (MODE == kBlock) {
+    if (C::PROMOTE) {
+      // Fold per-slab partials with compensated (Kahan) addition:
+      //   acc += w * partial,  w = a_s[m][kb] * b_s[nb][kb] (fp8 blockscale) or 1 (bf16).
+      // Each partial holds at most 128 K of products, so the fp32 rounding
+      // inside the tensor core stays at the scale of one slab, and the sum
+      // over slabs loses almost nothing.
+      float comp[kTokRows];
+#pragma unroll
+      for (int m = 0; m < kTokRows; ++m) comp[m] = 0.f;
       const float* a_s = static_cast<const float*>(p.a_scales);
       const int KS = p.K / 128;
       for (int i = 0; i < nslab; ++i) {
@@ -280,11 +294,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         __syncwarp();
         if (lane == 0) mbar_arrive(&pempty_bar[pb]);
         const int kb = u0 + i;
-        const float bsc = __ldg(p.b_s + static_cast<size_t>(nt) * KS + kb);
+        float bsc = 1.f;
+        if (MODE == kBlock) bsc = __ldg(p.b_s + static_cast<size_t>(nt) * KS + kb);
 #pragma unroll
         for (int m = 0; m < kTokRows; ++m) {
           const int row = mt * kTokRows + m;
-          if (row < p.M) acc[m] = fmaf(__ldg(a_s + static_cast<size_t>(row) * KS + kb) * bsc, __uint_as_float(v[m]), acc[m]);
+          float term = __uint_as_float(v[m]);
+          if (MODE == kBlock) term *= (row < p.M ? __ldg(a_s + static_cast<size_t>(row) * KS + kb) : 0.f) * bsc;
+          const float yk = term - comp[m];
+          const float t = acc[m] + yk;
+          comp[m] = (t - acc[m]) - yk;
+          acc[m] = t;
         }
       }
     } else {

