@@ -215,6 +215,31 @@ FG_API fg_status fg_gemm_splitk_reduce(const float* ws, int split_k, int64_t M, 
                                 const float* b_s, void* Y, void* stream);
 
 /*
+ * fg_gemm without a caller workspace (no counterpart in the pages).  For
+ * callers that cannot allocate device memory while they run -- a serving
+ * loop whose buffers are all sized at start-up (cudaMalloc can synchronise
+ * the device and stall every stream), or a plug-in whose host framework owns
+ * all device memory and offers no allocator.  The fp32 split-K partials go
+ * to an 8 MiB array that the library keeps in every device's memory until
+ * the process exits; this call allocates nothing.
+ *  - Arguments as fg_gemm, minus the workspace.  FG_FLAG_DEFER_REDUCE is
+ *    refused (FG_ERR_INVALID_ARG): the partials would stay in the private
+ *    scratch.
+ *  - A call whose split needs more than 8 MiB (split_k * M * N * 4 bytes) is
+ *    refused with FG_ERR_WORKSPACE before anything is launched.
+ *  - The first call on a device looks up the scratch's device address (once
+ *    per device, with that device current); make that first call before any
+ *    stream capture.
+ *  - All calls share the one array and it keeps the last call's partials.
+ *    Nothing in it has to start at zero (every split writes its whole
+ *    partial before the reduce reads it), but two calls that overlap on the
+ *    GPU (e.g. on two streams) race on it: serialise them.
+ * Errors: as fg_gemm.
+ */
+FG_API fg_status fg_gemm_noalloc(const void* A, const void* a_scales, int64_t M, const fg_bshuf* b, int mode,
+                                 int split_k, void* Y, uint32_t flags, void* stream);
+
+/*
  * Synchronises the current device and returns (and clears) the error word
  * the library's kernels write when a bounded wait runs out: FG_OK or
  * FG_ERR_TIMEOUT.  A failed synchronisation returns FG_ERR_CUDA.

@@ -66,6 +66,7 @@ def lib():
         "fg_gemm_workspace_size": ([i32, i64, i64, i64, i32, ctypes.POINTER(u64)], i32),
         "fg_gemm": ([vp, vp, i64, ctypes.POINTER(BShuf), i32, i32, vp, vp, u64, u32, vp], i32),
         "fg_gemm_splitk_reduce": ([vp, i32, i64, i64, vp, vp, vp, vp], i32),
+        "fg_gemm_noalloc": ([vp, vp, i64, ctypes.POINTER(BShuf), i32, i32, vp, u32, vp], i32),
         "fg_get_error": ([], i32),
         "fg_set_wait_timeout_ns": ([u64], None),
         "fg_debug_override_cc": ([i32, i32], None),
@@ -217,6 +218,18 @@ def gemm(A, pb, a_scales=None, mode=None, split_k=0, Y=None, workspace=None, fla
         ws_bytes = workspace.numel() * workspace.element_size()
     _check(lib().fg_gemm(_ptr(A), _ptr(a_scales), M, ctypes.byref(pb.desc), mode, split_k, _ptr(Y),
                          _ptr(workspace), ws_bytes, flags, _stream(stream)))
+    return Y
+
+
+def gemm_noalloc(A, pb, a_scales=None, mode=None, split_k=0, Y=None, flags=0, stream=None):
+    """gemm() for callers that cannot allocate device memory: the split-K
+    partials go to the library's built-in 8 MiB scratch (see fg_gemm_noalloc
+    in include/fg.h).  Y must be given by such a caller; returns Y."""
+    mode = pb.mode if mode is None else _mode(mode)
+    if Y is None:
+        Y = torch.empty((A.shape[0], pb.N), dtype=torch.bfloat16, device=A.device)
+    _check(lib().fg_gemm_noalloc(_ptr(A), _ptr(a_scales), A.shape[0], ctypes.byref(pb.desc), mode, split_k,
+                                 _ptr(Y), flags, _stream(stream)))
     return Y
 
 

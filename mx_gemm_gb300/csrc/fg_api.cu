@@ -235,6 +235,13 @@ fg_status make_tmap(CUtensorMap* map, const void* base, int64_t rows, int64_t rb
 
 }  // namespace
 
+void set_error_message(const char* fmt, ...) {
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(g_msg, sizeof g_msg, fmt, ap);
+  va_end(ap);
+}
+
 int sm_count() {
   static int count[64] = {};
   int dev = 0;

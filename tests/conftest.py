@@ -13,6 +13,16 @@ def pytest_configure(config):
     config.addinivalue_line("markers", "slow: long CPU-side oracle work")
 
 
+@pytest.fixture(scope="session", autouse=True)
+def _built_libraries():
+    """Build the CUDA library and the oracle if they are missing or stale
+    (a no-op when they are up to date)."""
+    from mx_gemm_gb300 import build as libbuild
+    from oracle import build as orcbuild
+    libbuild.build()
+    orcbuild.build()
+
+
 def pytest_collection_modifyitems(config, items):
     try:
         import torch
