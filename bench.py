@@ -4,7 +4,8 @@ Default workload: the FP8 e4m3 per-tensor split-K decode sweep the pages
 measure (M in {1,16} x N in {2048,16384}, K=7168; split_k from the dispatch
 table), one step = the four GEMMs (mainloop + split-K reduce) back to back.
 Metric: decode GEMM GB/s = algorithmic bytes (A + B + scales + Y) / time,
-whole job over all ranks.  Other workloads: --workload (see WORKLOADS).
+whole job over all ranks.  Other workloads (--workload): the other decode
+scale modes, and the large-M shapes (metric TFLOP/s = 2MNK / time).
 
 Prints one JSON line (rank 0).  ``--impl reference`` times the CPU oracle on
 the host cores instead (a bounded sample of the same workload per step).
@@ -38,6 +39,9 @@ def decode_cases(mode, K=7168):
 
 WORKLOADS = {
     "fp8_tensor_decode_sweep_k7168": dict(cases=decode_cases("fp8_tensor"), kind="decode", idx=1),
+    "large_bf16_54560x8192x8192": dict(cases=[dict(mode="bf16", M=54560, N=8192, K=8192)], kind="large", idx=3),
+    "large_fp8_4096x4096x8192": dict(cases=[dict(mode="fp8_tensor", M=4096, N=4096, K=8192)], kind="large",
+                                     idx=3, case_offset=1),
     "fp8_block128_decode_sweep_k7168": dict(cases=decode_cases("fp8_block128"), kind="decode", idx=2),
     "mxfp8_decode_n16384_k7168": dict(cases=[dict(mode="mxfp8", M=m, N=16384, K=7168) for m in (1, 16)],
                                       kind="decode", idx=4),
@@ -67,6 +71,18 @@ def algo_bytes(c, n=None):
     """A + B + scales + Y bytes of one GEMM (n restricts to the first n weight rows)."""
     M, N, K, mode = c["M"], c["N"] if n is None else n, c["K"], c["mode"]
     return int(M * K * elem_bytes(mode) + N * K * elem_bytes(mode) + scale_bytes(mode, M, N, K) + 2 * M * N)
+
+
+def algo_flops(c, n=None):
+    return 2.0 * c["M"] * (c["N"] if n is None else n) * c["K"]
+
+
+def work(kind, c, n=None):
+    """The metric's unit of work for one GEMM: bytes (decode) or flops (large)."""
+    return algo_flops(c, n) if kind == "large" else algo_bytes(c, n)
+
+
+METRIC = {"decode": ("decode GEMM GB/s", "GB/s", 1e9), "large": ("large GEMM TFLOP/s", "TFLOP/s", 1e12)}
 
 
 def case_operands(wl_idx, i, c):
@@ -161,7 +177,7 @@ class OracleSample:
                 bs = b_s[:n]
             self.oracle.gemm(self.orc[c["mode"]], A, B[:n], a_s, bs, M=c["M"], N=n, K=c["K"],
                              threads=self.threads)
-            nbytes += algo_bytes(c, n)
+            nbytes += work(self.wl["kind"], c, n)
         return time.perf_counter() - t0, nbytes
 
     def describe(self):
@@ -174,20 +190,27 @@ class OracleSample:
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=3000)
-    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=None, help="timed steps (default per workload)")
+    ap.add_argument("--warmup", type=int, default=None)
     ap.add_argument("--impl", default="fg", choices=["fg", "reference"])
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(WORKLOADS))
-    ap.add_argument("--rotate", type=int, default=3, help="weight copies cycled to keep L2 cold")
+    ap.add_argument("--rotate", type=int, default=None, help="operand copies cycled to keep L2 cold")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
-    if args.warmup < 3:
-        args.warmup = 3
+    wl = WORKLOADS[args.workload]
+    kind = wl["kind"]
+    if args.steps is None:
+        args.steps = 3000 if kind == "decode" else 40
+    if args.warmup is None:
+        args.warmup = 20 if kind == "decode" else 5
+    args.warmup = max(3, args.warmup)
+    if args.rotate is None:
+        args.rotate = 3 if kind == "decode" else (1 if wl["cases"][0]["M"] * wl["cases"][0]["K"] > 2e8 else 4)
+    metric, unit, scale_u = METRIC[kind]
 
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     local_rank = int(os.environ.get("LOCAL_RANK", "0"))
-    wl = WORKLOADS[args.workload]
     peaks = dict(FALLBACK_PEAKS)
     peaks_src = "fallback"
     if os.path.exists(PEAKS_FILE):
@@ -196,31 +219,33 @@ def main():
             peaks_src = "measured"
         except ValueError:
             pass
+    off = wl.get("case_offset", 0)
+    host_ops_fn = lambda: [case_operands(wl["idx"], i + off, c) for i, c in enumerate(wl["cases"])]  # noqa: E731
+    dtype = {"bf16": "bf16", "fp8_tensor": "e4m3", "fp8_block128": "e4m3", "mxfp8": "e4m3",
+             "mxfp4": "e2m1"}[wl["cases"][0]["mode"]]
 
     if args.impl == "reference":
         if rank != 0:
             return
-        host_ops = [case_operands(wl["idx"], i, c) for i, c in enumerate(wl["cases"])]
+        host_ops = host_ops_fn()
         budget = 90.0 / max(1, args.steps + args.warmup)   # whole run ~1.5 min
         ref = OracleSample(wl, host_ops, budget)
-        times, total_bytes = [], 0
+        times, total = [], 0.0
         for s in range(args.warmup + args.steps):
-            t, nb = ref.run()
+            t, nw = ref.run()
             if s >= args.warmup:
                 times.append(t)
-                total_bytes += nb
+                total += nw
         tsum = sum(times)
-        value = total_bytes / tsum / 1e9
-        threads = ref.threads
-        sample = ref.describe()
-        line = {"metric": "decode GEMM GB/s", "value": value, "unit": "GB/s", "impl": "reference",
+        value = total / tsum / scale_u
+        line = {"metric": metric, "value": value, "unit": unit, "impl": "reference",
                 "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
                 "ms_per_step": 1000 * tsum / len(times), "higher_is_better": True, "scaling": "weak",
                 "vs_baseline": None, "dtype": "f64", "data": "synthetic",
                 "config": {"workload": args.workload, "cases": wl["cases"]},
-                "cpu_baseline": {"value": value, "unit": "GB/s", "cores": threads, "kind": "oracle",
-                                 "sample": sample},
-                "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+                "cpu_baseline": {"value": value, "unit": unit, "cores": ref.threads, "kind": "oracle",
+                                 "sample": ref.describe()},
+                "e2e": {"value": value, "unit": unit, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
         print(json.dumps(line), flush=True)
         return
 
@@ -240,43 +265,45 @@ def main():
         x = np.ascontiguousarray(x)
         return torch.from_numpy(x.view(np.int16) if x.dtype == np.uint16 else x).to(dev)
 
-    # operands: one activation per case, `rotate` preshuffled copies of each weight
-    host_ops = [case_operands(wl["idx"], i, c) for i, c in enumerate(wl["cases"])]
+    # operands: `rotate` copies of every activation and preshuffled weight
+    host_ops = host_ops_fn()
     cases = []
     for c, (A, B, a_s, b_s) in zip(wl["cases"], host_ops):
         dB, db_s = to_dev(B), to_dev(b_s)
-        pbs = [fg.preshuffle_b(c["mode"], dB, db_s, K=c["K"]) for _ in range(max(1, args.rotate))]
+        R = max(1, args.rotate)
+        pbs = [fg.preshuffle_b(c["mode"], dB, db_s, K=c["K"]) for _ in range(R)]
         del dB
+        dA0 = to_dev(A)
+        dAs = [dA0] + [dA0.clone() for _ in range(R - 1 if kind == "large" else 0)]
         plan = fg.gemm_plan(c["mode"], c["M"], c["N"], c["K"])
         S = plan["split_k"]
-        ws = torch.empty(max(1, S * c["M"] * c["N"]), dtype=torch.float32, device=dev)
+        ws = torch.empty(max(1, S * c["M"] * c["N"] if S > 1 else 1), dtype=torch.float32, device=dev)
         Y = torch.empty((c["M"], c["N"]), dtype=torch.bfloat16, device=dev)
-        dA, da_s = to_dev(A), to_dev(a_s)
         hA = torch.from_numpy(np.ascontiguousarray(A).view(np.int16) if A.dtype == np.uint16 else
                               np.ascontiguousarray(A)).pin_memory()
         ha_s = torch.from_numpy(np.ascontiguousarray(a_s)).pin_memory() if a_s is not None else None
         hY = torch.empty((c["M"], c["N"]), dtype=torch.bfloat16).pin_memory()
-        red_as = da_s if c["mode"] == "fp8_tensor" else None
-        red_bs = pbs[0].sf[:4].view(torch.float32) if c["mode"] == "fp8_tensor" else None
-        cases.append(dict(c=c, pbs=pbs, S=S, ws=ws, Y=Y, dA=dA, da_s=da_s, hA=hA, ha_s=ha_s, hY=hY,
-                          plan=plan, bytes=algo_bytes(c), red_as=red_as, red_bs=red_bs))
+        red_as = to_dev(a_s) if c["mode"] == "fp8_tensor" else None
+        cases.append(dict(c=c, pbs=pbs, dAs=dAs, S=S, ws=ws, Y=Y, da_s=to_dev(a_s), hA=hA, ha_s=ha_s,
+                          hY=hY, plan=plan, work=work(kind, c), red_as=red_as))
     torch.cuda.synchronize()
 
     def one_case(x, r, ev=None):
         st = torch.cuda.current_stream()
         pb = x["pbs"][r % len(x["pbs"])]
+        dA = x["dAs"][r % len(x["dAs"])]
         S = x["S"]
         if ev is not None:
             ev[0].record(st)
         if S > 1:
-            fg.gemm(x["dA"], pb, x["da_s"], split_k=S, Y=x["Y"], workspace=x["ws"],
+            fg.gemm(dA, pb, x["da_s"], split_k=S, Y=x["Y"], workspace=x["ws"],
                     flags=fg.FG_FLAG_DEFER_REDUCE, stream=st)
             if ev is not None:
                 ev[1].record(st)
             rs = pb.sf[:4].view(torch.float32) if x["c"]["mode"] == "fp8_tensor" else None
             fg.gemm_splitk_reduce(x["ws"], S, x["c"]["M"], x["c"]["N"], x["red_as"], rs, Y=x["Y"], stream=st)
         else:
-            fg.gemm(x["dA"], pb, x["da_s"], split_k=1, Y=x["Y"], stream=st)
+            fg.gemm(dA, pb, x["da_s"], split_k=1, Y=x["Y"], stream=st)
             if ev is not None:
                 ev[1].record(st)
 
@@ -337,10 +364,10 @@ def main():
         ms = float(tt.item())
     if fg.get_error() != fg.FG_OK:
         raise RuntimeError("kernel error word set during the timed region")
-    step_bytes = sum(x["bytes"] for x in cases)
-    value = world * K * step_bytes / (ms / 1e3) / 1e9
+    step_work = sum(x["work"] for x in cases)
+    value = world * K * step_work / (ms / 1e3) / scale_u
 
-    # dominant kernel: the mainloop (decode) kernel over all cases
+    # dominant kernel: the mainloop kernel over all cases (reduce excluded)
     main_ms = [0.0] * len(cases)
     for s in range(K):
         for i in range(len(cases)):
@@ -348,12 +375,18 @@ def main():
     per_case = []
     for i, x in enumerate(cases):
         avg = main_ms[i] / K
-        per_case.append({"M": x["c"]["M"], "N": x["c"]["N"], "K": x["c"]["K"], "split_k": x["S"],
-                         "kernel": x["plan"]["name"], "mainloop_us": round(avg * 1e3, 3),
-                         "mainloop_gbs": round(x["bytes"] / (avg / 1e3) / 1e9, 1)})
-    main_avg_s = sum(main_ms) / K / 1e3
-    achieved = step_bytes / main_avg_s / 1e9
-    peak = float(peaks["hbm_gbs"])
+        per_case.append({"mode": x["c"]["mode"], "M": x["c"]["M"], "N": x["c"]["N"], "K": x["c"]["K"],
+                         "split_k": x["S"], "kernel": x["plan"]["name"], "mainloop_us": round(avg * 1e3, 3),
+                         "mainloop_" + unit.replace("/", "p"): round(x["work"] / (avg / 1e3) / scale_u, 1)})
+    achieved = step_work / (sum(main_ms) / K / 1e3) / scale_u
+    if kind == "decode":
+        bound, peak, psrc = "hbm", float(peaks["hbm_gbs"]), peaks_src + " hbm_gbs (burst copy)"
+    else:
+        # a seconds-long loop of one contraction: the sustained bf16 figure;
+        # fp8 runs at twice the bf16 rate (nominal 4.5 vs 2.25 PFLOP/s dense)
+        ratio = 1.0 if dtype == "bf16" else 2.0
+        bound, peak = "tensor", ratio * float(peaks["bf16_tflops_sustained"])
+        psrc = peaks_src + " bf16_tflops_sustained" + (" x 2 (fp8/bf16 nominal ratio)" if ratio != 1 else "")
 
     # ---------------- end-to-end: host buffers, H2D of A, D2H of Y in the region
     E = max(3, K // 10)
@@ -366,7 +399,7 @@ def main():
     e0.record(stream)
     for s in range(E):
         for x in cases:
-            x["dA"].copy_(x["hA"], non_blocking=True)
+            x["dAs"][s % len(x["dAs"])].copy_(x["hA"], non_blocking=True)
             if x["ha_s"] is not None:
                 x["da_s"].copy_(x["ha_s"], non_blocking=True)
             one_case(x, s)
@@ -374,42 +407,39 @@ def main():
     e1.record(stream)
     torch.cuda.synchronize()
     e2e_ms = e0.elapsed_time(e1)
-    e2e_value = world * E * step_bytes / (e2e_ms / 1e3) / 1e9
+    e2e_value = world * E * step_work / (e2e_ms / 1e3) / scale_u
 
     launches_per_step = sum(2 if x["S"] > 1 else 1 for x in cases)
 
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
         ref = OracleSample(wl, host_ops, 15.0)
-        t, nb = ref.run()
-        cpu = {"value": nb / t / 1e9, "unit": "GB/s", "cores": ref.threads, "kind": "oracle",
+        t, nw = ref.run()
+        cpu = {"value": nw / t / scale_u, "unit": unit, "cores": ref.threads, "kind": "oracle",
                "sample": ref.describe() + ", one pass of %.1f s" % t}
 
     if rank == 0:
+        wbytes = sum(x["c"]["N"] * x["c"]["K"] * elem_bytes(x["c"]["mode"]) for x in cases)
+        abytes = sum(x["c"]["M"] * x["c"]["K"] * elem_bytes(x["c"]["mode"]) for x in cases)
         line = {
-            "metric": "decode GEMM GB/s", "value": value, "unit": "GB/s", "n_gpus": world, "steps": K,
+            "metric": metric, "value": value, "unit": unit, "n_gpus": world, "steps": K,
             "warmup": args.warmup, "ms_per_step": ms / K, "higher_is_better": True,
-            "scaling": "weak", "vs_baseline": None, "dtype": "e4m3" if "fp8" in args.workload else
-            ("e2m1" if "mxfp4" in args.workload else "e4m3"),
-            "data": "synthetic",
-            "config": {"workload": args.workload, "K": 7168,
-                       "shapes": [[x["c"]["M"], x["c"]["N"]] for x in cases],
-                       "l2": "inputs larger than L2: %d distinct preshuffled weight copies, %.0f MB of weights "
-                             "per step, each weight reused only after the others" %
-                             (args.rotate * len(cases), args.rotate * sum(x["c"]["N"] * x["c"]["K"] *
-                                                                            elem_bytes(x["c"]["mode"])
-                                                                            for x in cases) / 1e6),
+            "scaling": "weak", "vs_baseline": None, "dtype": dtype, "data": "synthetic",
+            "config": {"workload": args.workload,
+                       "shapes": [[x["c"]["M"], x["c"]["N"], x["c"]["K"]] for x in cases],
+                       "l2": "inputs larger than L2: %d rotating copies, %.0f MB of operands cycled per %d steps"
+                             % (args.rotate, args.rotate * (wbytes + (abytes if kind == "large" else 0)) / 1e6,
+                                args.rotate),
                        "parallelism": "replicas" if world > 1 else "single"},
             "per_case": per_case,
-            "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
-                         "frac": round(achieved / peak, 4), "traffic": None,
-                         "peak_source": peaks_src + " hbm_gbs (burst copy)",
-                         "kernel": "decode mainloop (all cases, reduce excluded)"},
+            "roofline": {"bound": bound, "achieved": round(achieved, 1), "peak": peak, "unit": unit,
+                         "frac": round(achieved / peak, 4), "traffic": None, "peak_source": psrc,
+                         "kernel": "mainloop kernel (all cases, reduce excluded)"},
             "cpu_baseline": cpu,
-            "e2e": {"value": e2e_value, "unit": "GB/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+            "e2e": {"value": e2e_value, "unit": unit, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
             "gpu_launches": launches_per_step * K,
             "clocks": clocks,
-            "timed_region": "one CUDA-graph replay of the %d steps" % K if graph is not None else "eager launches",
+            "timed_region": ("one CUDA-graph replay of the %d steps" % K) if graph is not None else "eager launches",
         }
         print(json.dumps(line), flush=True)
     if world > 1:

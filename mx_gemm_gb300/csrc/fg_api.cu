@@ -142,7 +142,7 @@ const TableRow kTable[] = {
     {FG_FP8_BLOCK128, 1, 16384, 7168, 1, 2, 5}, {FG_FP8_BLOCK128, 16, 16384, 7168, 1, 2, 5},
 };
 
-int64_t decode_row_limit() { return 16; }
+int64_t decode_row_limit() { return 32; }
 
 fg_status make_plan(int mode, int64_t M, int64_t N, int64_t K, int split_k, fg_plan* out) {
   memset(out, 0, sizeof *out);

@@ -1,11 +1,256 @@
-// Large-M preshuffled-weight GEMM (placeholder until the tcgen05 kernel lands).
+// Large-M preshuffled-weight GEMM for sm_103a: the compute-bound form of the
+// FlyDSL PR "Enable the gmem->LDS async copy for f16/bf16 preshuffle GEMM"
+// (Performance: bf16 M=54560, N=K=8192) and of the fp8 shape in the FlyDSL PR
+// "Migrate kernels to fx.copy / .llvm_ptr" (Validation: M=N=4096, K=8192).
+//
+// Persistent kernel, one CTA per SM, 128 x 256 output tiles (A rows on the
+// MMA M side, two 128-row weight slabs on the N side).  Per 128-byte K slab
+// the producer issues one TMA load of the A tile (128 rows x 128 bytes,
+// 128-byte swizzle, rows past M read as zero) and one bulk copy per weight
+// slab (16 KiB each, already in the swizzled image layout), into a 4-stage
+// ring.  The MMA thread issues four tcgen05.mma (128 x 256 x 32 bytes of K)
+// per slab into one of two TMEM accumulators (256 fp32 columns each), so the
+// four epilogue warps can drain tile t (TMEM -> registers -> scale -> bf16 ->
+// global) while tile t+1 accumulates -- the issue-rate lesson of the FlyDSL
+// pages (A-fragment reads interleaved with the MMAs, async copies instead of
+// register round trips) in tcgen05 form.
+//
+// Tile order: tiles are walked in groups of `group_n` weight tiles; inside a
+// group the weight tile index runs fastest, so the CTAs resident at one time
+// share a band of weights (kept in L2) and a few A row blocks.
+#include <cuda_bf16.h>
+
 #include "fg_internal.cuh"
+#include "fg_ptx.cuh"
 
 namespace fg {
 
-bool large_supported(int) { return false; }
+namespace {
 
-cudaError_t launch_large(int, const CUtensorMap&, const LargeParams&, int, cudaStream_t) {
+constexpr int kThreads = 192;
+constexpr int kBM = 128;
+constexpr int kBN = 256;
+constexpr int kStages = 4;
+constexpr int kABytes = kBM * 128;        // 16 KiB
+constexpr int kBBytes = kBN * 128;        // 32 KiB
+constexpr int kStageBytes = kABytes + kBBytes;
+constexpr int kSmem = kStages * kStageBytes + 1024;
+constexpr int kTmemCols = 512;            // two 256-column accumulators
+constexpr int kGroupN = 16;
+
+static_assert(kSmem <= 232448, "shared memory budget");
+
+struct TileCoord {
+  int m, n;
+};
+
+__device__ __forceinline__ TileCoord tile_coord(int t, int tiles_m, int tiles_n) {
+  const int per_group = kGroupN * tiles_m;
+  const int g = t / per_group;
+  const int r = t - g * per_group;
+  const int gn = min(kGroupN, tiles_n - g * kGroupN);
+  TileCoord c;
+  c.m = r / gn;
+  c.n = g * kGroupN + (r - c.m * gn);
+  return c;
+}
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+  const __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<const uint32_t*>(&v);
+}
+
+template <int MODE>
+__global__ void __launch_bounds__(kThreads, 1)
+    large_kernel(const __grid_constant__ CUtensorMap tmap_a, const LargeParams p) {
+  extern __shared__ uint8_t dsmem[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(dsmem) + 1023) & ~uintptr_t(1023));
+  __shared__ __align__(8) uint64_t full_bar[kStages];
+  __shared__ __align__(8) uint64_t empty_bar[kStages];
+  __shared__ __align__(8) uint64_t accf_bar[2];
+  __shared__ __align__(8) uint64_t acce_bar[2];
+  __shared__ __align__(8) uint64_t stall_bar, drain_bar;
+  __shared__ uint32_t tmem_base_sh;
+  __shared__ int abort_sh, issued_sh, consumed_sh, mma_any_sh;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int tiles = p.tiles_m * p.tiles_n;
+  const int KB = p.KB;
+  const uint64_t T = p.timeout_ns;
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < kStages; ++i) {
+      mbar_init(&full_bar[i], 1);
+      mbar_init(&empty_bar[i], 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&accf_bar[i], 1);
+      mbar_init(&acce_bar[i], 4);
+    }
+    mbar_init(&stall_bar, 1);
+    mbar_init(&drain_bar, 1);
+    abort_sh = 0;
+    issued_sh = 0;
+    consumed_sh = 0;
+    mma_any_sh = 0;
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(&tmem_base_sh, kTmemCols);
+    tmem_relinquish();
+  }
+  if (warp == 0 && lane == 0) prefetch_tmap(&tmap_a);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = tmem_base_sh;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      int it = 0;
+      bool ok = true;
+      for (int t = blockIdx.x; ok && t < tiles; t += gridDim.x) {
+        const TileCoord tc = tile_coord(t, p.tiles_m, p.tiles_n);
+        const int nslabs_n = min(2, p.N / 128 - 2 * tc.n);  // weight slabs in this tile (1 or 2)
+        for (int kb = 0; kb < KB; ++kb, ++it) {
+          const int slot = it % kStages;
+          if (!mbar_wait(&empty_bar[slot], ((it / kStages) & 1) ^ 1u, T, p.err, 11)) {
+            ok = false;
+            break;
+          }
+          uint8_t* st = smem + slot * kStageBytes;
+          mbar_arrive_expect_tx(&full_bar[slot], kABytes + nslabs_n * 16384);
+          tma_load_2d(st, &tmap_a, kb * 128, tc.m * kBM, &full_bar[slot]);
+          for (int h = 0; h < nslabs_n; ++h)
+            bulk_g2s(st + kABytes + h * 16384,
+                     p.b_img + (static_cast<size_t>(2 * tc.n + h) * KB + kb) * 16384, 16384, &full_bar[slot]);
+        }
+      }
+      issued_sh = it;
+      if (!ok) abort_sh = 1;
+    }
+  } else if (warp == 1) {
+    // ---------------------------------------------------------- MMA issuer
+    if (lane == 0) {
+      bool ok = true;
+      if (p.debug_stall) ok = mbar_wait(&stall_bar, 0, T, p.err, 12);
+      int it = 0, ti = 0;
+      const uint32_t idesc = MODE == kBF16 ? idesc_bf16(kBM, kBN) : idesc_e4m3(kBM, kBN);
+      for (int t = blockIdx.x; ok && t < tiles; t += gridDim.x, ++ti) {
+        const int acc = ti & 1;
+        if (!mbar_wait(&acce_bar[acc], ((ti >> 1) & 1) ^ 1u, T, p.err, 13)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t d = tmem + acc * kBN;
+        for (int kb = 0; kb < KB; ++kb, ++it) {
+          const int slot = it % kStages;
+          if (!mbar_wait(&full_bar[slot], (it / kStages) & 1, T, p.err, 14)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          mma_any_sh = 1;
+          uint8_t* st = smem + slot * kStageBytes;
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            const uint64_t adesc = sdesc_sw128(smem_u32(st + j * 32));
+            const uint64_t bdesc = sdesc_sw128(smem_u32(st + kABytes + j * 32));
+            if (MODE == kBF16)
+              mma_f16(d, adesc, bdesc, idesc, (kb | j) != 0);
+            else
+              mma_f8f6f4(d, adesc, bdesc, idesc, (kb | j) != 0);
+          }
+          tc_commit(&empty_bar[slot]);
+        }
+        if (!ok) {
+          ++it;
+          break;
+        }
+        tc_commit(&accf_bar[acc]);
+      }
+      consumed_sh = it;
+      if (!ok) abort_sh = 1;
+      if (mma_any_sh) {
+        tc_commit(&drain_bar);
+        mbar_wait(&drain_bar, 0, T, p.err, 15);
+      }
+    }
+  } else {
+    // ------------------------------------------------------------ epilogue
+    const int qd = warp & 3;
+    float scale = 1.f;
+    if (MODE == kTensor) scale = __ldg(static_cast<const float*>(p.a_scales)) * __ldg(p.b_s);
+    int ti = 0;
+    for (int t = blockIdx.x; t < tiles; t += gridDim.x, ++ti) {
+      const int acc = ti & 1;
+      const bool w = mbar_wait(&accf_bar[acc], (ti >> 1) & 1, T, p.err, 16);
+      if (!__all_sync(0xffffffffu, w)) {
+        if (lane == 0) abort_sh = 1;
+        break;
+      }
+      tc_fence_after();
+      const TileCoord tc = tile_coord(t, p.tiles_m, p.tiles_n);
+      const int row = tc.m * kBM + qd * 32 + lane;
+      const int ncols = min(kBN, p.N - tc.n * kBN);
+      __nv_bfloat16* yrow = p.y + static_cast<size_t>(row) * p.N + static_cast<size_t>(tc.n) * kBN;
+      const uint32_t taddr = tmem + acc * kBN + (static_cast<uint32_t>(qd * 32) << 16);
+      for (int c = 0; c < ncols; c += 32) {
+        uint32_t v[32];
+        tmem_ld32(taddr + c, v);
+        tmem_wait_ld();
+        if (row < p.M) {
+          uint4* dst = reinterpret_cast<uint4*>(yrow + c);
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            uint4 o;
+            o.x = pack_bf16x2(__uint_as_float(v[8 * q + 0]) * scale, __uint_as_float(v[8 * q + 1]) * scale);
+            o.y = pack_bf16x2(__uint_as_float(v[8 * q + 2]) * scale, __uint_as_float(v[8 * q + 3]) * scale);
+            o.z = pack_bf16x2(__uint_as_float(v[8 * q + 4]) * scale, __uint_as_float(v[8 * q + 5]) * scale);
+            o.w = pack_bf16x2(__uint_as_float(v[8 * q + 6]) * scale, __uint_as_float(v[8 * q + 7]) * scale);
+            dst[q] = o;
+          }
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&acce_bar[acc]);
+    }
+  }
+
+  // ------------------------------------------------------------- teardown
+  tc_fence_before();
+  __syncthreads();
+  if (abort_sh && threadIdx.x == 0) {
+    for (int it = consumed_sh; it < issued_sh; ++it)
+      mbar_wait(&full_bar[it % kStages], (it / kStages) & 1, T, nullptr, 0);
+  }
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 1) tmem_dealloc(tmem, kTmemCols);
+}
+
+template <int MODE>
+cudaError_t launch_mode(const CUtensorMap& tmap_a, const LargeParams& p, int ctas, cudaStream_t stream) {
+  static bool attr_set = false;
+  if (!attr_set) {
+    cudaError_t e = cudaFuncSetAttribute(large_kernel<MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
+    if (e != cudaSuccess) return e;
+    attr_set = true;
+  }
+  large_kernel<MODE><<<ctas, kThreads, kSmem, stream>>>(tmap_a, p);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+bool large_supported(int mode) { return mode == kBF16 || mode == kTensor; }
+
+cudaError_t launch_large(int mode, const CUtensorMap& tmap_a, const LargeParams& p, int ctas, cudaStream_t stream) {
+  if (mode == kBF16) return launch_mode<kBF16>(tmap_a, p, ctas, stream);
+  if (mode == kTensor) return launch_mode<kTensor>(tmap_a, p, ctas, stream);
   return cudaErrorNotSupported;
 }
 
