@@ -46,7 +46,11 @@ WORKLOADS = {
     "mxfp8_decode_n16384_k7168": dict(cases=[dict(mode="mxfp8", M=m, N=16384, K=7168) for m in (1, 16)],
                                       kind="decode", idx=4),
     "mxfp4_decode_n16384_k7168": dict(cases=[dict(mode="mxfp4", M=m, N=16384, K=7168) for m in (1, 16)],
-                                      kind="decode", idx=4),
+                                      kind="decode", idx=4, case_offset=3),
+    "large_mxfp8_4096x16384x7168": dict(cases=[dict(mode="mxfp8", M=4096, N=16384, K=7168)], kind="large",
+                                        idx=4, case_offset=2),
+    "large_mxfp4_4096x16384x7168": dict(cases=[dict(mode="mxfp4", M=4096, N=16384, K=7168)], kind="large",
+                                        idx=4, case_offset=5),
 }
 DEFAULT_WORKLOAD = "fp8_tensor_decode_sweep_k7168"
 
@@ -185,6 +189,36 @@ class OracleSample:
             "/".join(str(self.rows(c)) for c in self.wl["cases"]), len(self.wl["cases"]))
 
 
+# ----------------------------------------------------------- ncu traffic
+
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "traffic.json")
+
+
+def kernel_sources_digest(fg):
+    """Digest of the library's kernel sources, to tell whether a stored ncu
+    traffic figure still describes the kernels being timed."""
+    import hashlib
+    h = hashlib.sha256()
+    csrc = os.path.join(os.path.dirname(fg.__file__), "csrc")
+    for name in sorted(os.listdir(csrc)):
+        if name.endswith((".cu", ".cuh")):
+            h.update(name.encode())
+            h.update(open(os.path.join(csrc, name), "rb").read())
+    return h.hexdigest()[:16]
+
+
+def traffic(workload, fg):
+    """DRAM bytes (read + write) per step of the dominant kernel from the
+    committed ncu summary, or None when there is none for these sources."""
+    try:
+        rec = json.load(open(TRAFFIC_FILE)).get(workload)
+    except (OSError, ValueError):
+        return None
+    if not rec or rec.get("sources") != kernel_sources_digest(fg):
+        return None
+    return rec.get("dram_bytes_per_step")
+
+
 # ------------------------------------------------------------------- main
 
 def main():
@@ -277,7 +311,8 @@ def main():
         dAs = [dA0] + [dA0.clone() for _ in range(R - 1 if kind == "large" else 0)]
         plan = fg.gemm_plan(c["mode"], c["M"], c["N"], c["K"])
         S = plan["split_k"]
-        ws = torch.empty(max(1, S * c["M"] * c["N"] if S > 1 else 1), dtype=torch.float32, device=dev)
+        ws_bytes = fg.gemm_workspace_size(c["mode"], c["M"], c["N"], c["K"])
+        ws = torch.empty(max(4, ws_bytes) // 4, dtype=torch.float32, device=dev)
         Y = torch.empty((c["M"], c["N"]), dtype=torch.bfloat16, device=dev)
         hA = torch.from_numpy(np.ascontiguousarray(A).view(np.int16) if A.dtype == np.uint16 else
                               np.ascontiguousarray(A)).pin_memory()
@@ -288,28 +323,39 @@ def main():
                           hY=hY, plan=plan, work=work(kind, c), red_as=red_as))
     torch.cuda.synchronize()
 
-    def one_case(x, r, ev=None):
+    def one_case(x, r):
         st = torch.cuda.current_stream()
         pb = x["pbs"][r % len(x["pbs"])]
         dA = x["dAs"][r % len(x["dAs"])]
-        S = x["S"]
-        if ev is not None:
-            ev[0].record(st)
-        if S > 1:
-            fg.gemm(dA, pb, x["da_s"], split_k=S, Y=x["Y"], workspace=x["ws"],
-                    flags=fg.FG_FLAG_DEFER_REDUCE, stream=st)
-            if ev is not None:
-                ev[1].record(st)
-            rs = pb.sf[:4].view(torch.float32) if x["c"]["mode"] == "fp8_tensor" else None
-            fg.gemm_splitk_reduce(x["ws"], S, x["c"]["M"], x["c"]["N"], x["red_as"], rs, Y=x["Y"], stream=st)
-        else:
-            fg.gemm(dA, pb, x["da_s"], split_k=1, Y=x["Y"], stream=st)
-            if ev is not None:
-                ev[1].record(st)
+        fg.gemm(dA, pb, x["da_s"], split_k=x["S"], Y=x["Y"], workspace=x["ws"], stream=st)
 
-    def step(r, evs=None):
-        for i, x in enumerate(cases):
-            one_case(x, r, None if evs is None else evs[i])
+    def step(r):
+        for x in cases:
+            one_case(x, r)
+
+    def graph_of(fn, n):
+        """Capture fn(0..n-1) into one CUDA graph (the launches of a decode
+        step are short enough that host launch latency would otherwise show)."""
+        g = torch.cuda.CUDAGraph()
+        cap = torch.cuda.Stream()
+        cap.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.graph(g, stream=cap):
+            for r in range(n):
+                fn(r)
+        torch.cuda.synchronize()
+        g.replay()                          # one untimed replay
+        torch.cuda.synchronize()
+        return g
+
+    def time_graph(g):
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        st = torch.cuda.current_stream()
+        e0.record(st)
+        g.replay()
+        e1.record(st)
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1)
 
     for w in range(args.warmup):
         step(w)
@@ -317,26 +363,9 @@ def main():
     if fg.get_error() != fg.FG_OK:
         raise RuntimeError("kernel error word set during warm-up")
 
-    # The K timed steps are captured once into a CUDA graph (a decode step is
-    # launch-bound on the host otherwise) with timing events around every
-    # mainloop launch, then replayed once inside the timed region.
+    # ---------------- timed region: one replay of a graph of the K steps
     K = args.steps
-    graph = None
-    try:
-        evs = [[[torch.cuda.Event(enable_timing=True, external=True) for _ in range(2)] for _ in cases]
-               for _ in range(K)]
-        graph = torch.cuda.CUDAGraph()
-        cap = torch.cuda.Stream()
-        cap.wait_stream(torch.cuda.current_stream())
-        with torch.cuda.graph(graph, stream=cap):
-            for s in range(K):
-                step(s, evs[s])
-        torch.cuda.synchronize()
-        graph.replay()                      # one untimed replay
-        torch.cuda.synchronize()
-    except TypeError:
-        graph = None
-        evs = [[[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in cases] for _ in range(K)]
+    graph = graph_of(step, K)
     stream = torch.cuda.current_stream()
     clk = ClockSampler(local_rank)
     clk.start()
@@ -347,17 +376,14 @@ def main():
     t0 = torch.cuda.Event(enable_timing=True)
     t1 = torch.cuda.Event(enable_timing=True)
     t0.record(stream)
-    if graph is not None:
-        graph.replay()
-    else:
-        for s in range(K):
-            step(s, evs[s])
+    graph.replay()
     t1.record(stream)
     torch.cuda.synchronize()
     if world > 1:
         dist.barrier()
     clocks = clk.stop()
     ms = t0.elapsed_time(t1)
+    del graph
     if world > 1:
         tt = torch.tensor([ms], device=dev)
         dist.all_reduce(tt, op=dist.ReduceOp.MAX)
@@ -367,26 +393,29 @@ def main():
     step_work = sum(x["work"] for x in cases)
     value = world * K * step_work / (ms / 1e3) / scale_u
 
-    # dominant kernel: the mainloop kernel over all cases (reduce excluded)
-    main_ms = [0.0] * len(cases)
-    for s in range(K):
-        for i in range(len(cases)):
-            main_ms[i] += evs[s][i][0].elapsed_time(evs[s][i][1])
-    per_case = []
-    for i, x in enumerate(cases):
-        avg = main_ms[i] / K
+    # ---------------- per case: the main kernel alone, back to back (a graph
+    # of the same call repeated, CUDA events around its replay)
+    per_case, main_ms = [], []
+    for x in cases:
+        n = max(20, min(K, 400))
+        g = graph_of(lambda r, x=x: one_case(x, r), n)
+        avg = time_graph(g) / n
+        del g
+        main_ms.append(avg)
         per_case.append({"mode": x["c"]["mode"], "M": x["c"]["M"], "N": x["c"]["N"], "K": x["c"]["K"],
-                         "split_k": x["S"], "kernel": x["plan"]["name"], "mainloop_us": round(avg * 1e3, 3),
-                         "mainloop_" + unit.replace("/", "p"): round(x["work"] / (avg / 1e3) / scale_u, 1)})
-    achieved = step_work / (sum(main_ms) / K / 1e3) / scale_u
+                         "split_k": x["S"], "kernel": x["plan"]["name"], "us": round(avg * 1e3, 3),
+                         unit.replace("/", "p"): round(x["work"] / (avg / 1e3) / scale_u, 1)})
+    achieved = step_work / (sum(main_ms) / 1e3) / scale_u
     if kind == "decode":
         bound, peak, psrc = "hbm", float(peaks["hbm_gbs"]), peaks_src + " hbm_gbs (burst copy)"
     else:
-        # a seconds-long loop of one contraction: the sustained bf16 figure;
-        # fp8 runs at twice the bf16 rate (nominal 4.5 vs 2.25 PFLOP/s dense)
-        ratio = 1.0 if dtype == "bf16" else 2.0
+        # a seconds-long loop of one contraction: the sustained bf16 figure,
+        # times the nominal dense ratio of the operand type (fp8 4.5 and fp4
+        # 13.5 vs bf16 2.25 PFLOP/s)
+        ratio = {"bf16": 1.0, "e4m3": 2.0, "e2m1": 6.0}[dtype]
         bound, peak = "tensor", ratio * float(peaks["bf16_tflops_sustained"])
-        psrc = peaks_src + " bf16_tflops_sustained" + (" x 2 (fp8/bf16 nominal ratio)" if ratio != 1 else "")
+        psrc = peaks_src + " bf16_tflops_sustained" + (
+            " x %g (%s/bf16 nominal dense ratio)" % (ratio, dtype) if ratio != 1 else "")
 
     # ---------------- end-to-end: host buffers, H2D of A, D2H of Y in the region
     E = max(3, K // 10)
@@ -409,7 +438,9 @@ def main():
     e2e_ms = e0.elapsed_time(e1)
     e2e_value = world * E * step_work / (e2e_ms / 1e3) / scale_u
 
-    launches_per_step = sum(2 if x["S"] > 1 else 1 for x in cases)
+    launches_per_step = sum((2 if x["S"] > 8 else 1) + (1 if x["plan"]["path"] == 1 and
+                                                        x["c"]["mode"] in ("mxfp8", "mxfp4") else 0)
+                            for x in cases)
 
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
@@ -433,13 +464,15 @@ def main():
                        "parallelism": "replicas" if world > 1 else "single"},
             "per_case": per_case,
             "roofline": {"bound": bound, "achieved": round(achieved, 1), "peak": peak, "unit": unit,
-                         "frac": round(achieved / peak, 4), "traffic": None, "peak_source": psrc,
-                         "kernel": "mainloop kernel (all cases, reduce excluded)"},
+                         "frac": round(achieved / peak, 4), "traffic": traffic(args.workload, fg),
+                         "peak_source": psrc,
+                         "kernel": "the GEMM's main kernel, per case timed back to back, work summed over "
+                                   "the cases"},
             "cpu_baseline": cpu,
             "e2e": {"value": e2e_value, "unit": unit, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
             "gpu_launches": launches_per_step * K,
             "clocks": clocks,
-            "timed_region": ("one CUDA-graph replay of the %d steps" % K) if graph is not None else "eager launches",
+            "timed_region": "one CUDA-graph replay of the %d steps" % K,
         }
         print(json.dumps(line), flush=True)
     if world > 1:

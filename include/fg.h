@@ -178,7 +178,14 @@ FG_API fg_status fg_unshuffle_b(const fg_bshuf* desc, void* B_out, void* b_scale
  */
 FG_API fg_status fg_gemm_plan(int mode, int64_t M, int64_t N, int64_t K, int split_k, fg_plan* out);
 
-/* Workspace bytes fg_gemm needs for this shape and split (0 when split_k resolves to 1). */
+/*
+ * Workspace bytes a call of fg_gemm without FG_FLAG_DEFER_REDUCE needs for
+ * this shape and split: 0 when the split resolves to 1 or to at most 8 (the
+ * splits of a tile then reduce inside one thread-block cluster, with no
+ * global scratch), split_k*M*N*4 for larger splits, and the A scale image
+ * for large-M MX shapes.  A call with FG_FLAG_DEFER_REDUCE always needs
+ * split_k*M*N*4 bytes.
+ */
 FG_API fg_status fg_gemm_workspace_size(int mode, int64_t M, int64_t N, int64_t K, int split_k, uint64_t* bytes);
 
 /*
@@ -192,11 +199,14 @@ FG_API fg_status fg_gemm_workspace_size(int mode, int64_t M, int64_t N, int64_t 
  *           the contiguous run of 128-byte K slabs [s*q + min(s,r), ...) of
  *           length q + (s < r), q = U/S, r = U%S, U = Kb/128.
  *  Y        device bf16 [M][N].
- *  workspace / workspace_bytes: device fp32 [split_k][M][N] when the
- *           resolved split_k > 1 (see fg_gemm_workspace_size); may be NULL
- *           otherwise.  It holds, per split, the partial sum: unscaled for
- *           FP8_TENSOR (the per-tensor scale is applied once, in the reduce),
- *           fully scaled for the other modes.
+ *  workspace / workspace_bytes: as fg_gemm_workspace_size says; may be
+ *           NULL when that is 0.  With FG_FLAG_DEFER_REDUCE (or a split
+ *           above 8) it holds fp32 [split_k][M][N], per split the partial
+ *           sum: unscaled for FP8_TENSOR (the per-tensor scale is applied
+ *           once, in the reduce), fully scaled for the other modes.  Splits
+ *           of 2..8 without the flag sum their partials in split order
+ *           inside one thread-block cluster, which gives the same bits as
+ *           the workspace + fg_gemm_splitk_reduce pair.
  *  flags    FG_FLAG_DEFER_REDUCE: leave the partials in the workspace and do
  *           not write Y (call fg_gemm_splitk_reduce later).
  * Errors: INVALID_ARG, SHAPE, ALIGN, LAYOUT, WORKSPACE, UNSUPPORTED_ARCH, CUDA.
@@ -221,7 +231,8 @@ FG_API fg_status fg_gemm_splitk_reduce(const float* ws, int split_k, int64_t M, 
  * the device and stall every stream), or a plug-in whose host framework owns
  * all device memory and offers no allocator.  The fp32 split-K partials go
  * to an 8 MiB array that the library keeps in every device's memory until
- * the process exits; this call allocates nothing.
+ * the process exits (used by calls whose split needs a workspace, i.e.
+ * splits above 8); this call allocates nothing.
  *  - Arguments as fg_gemm, minus the workspace.  FG_FLAG_DEFER_REDUCE is
  *    refused (FG_ERR_INVALID_ARG): the partials would stay in the private
  *    scratch.

@@ -136,13 +136,17 @@ struct TableRow {
 // Exact-shape rows (decode shapes measured on this part); anything else
 // falls through to the heuristic below.
 const TableRow kTable[] = {
-    {FG_FP8_TENSOR, 1, 2048, 7168, 8, 1, 8},   {FG_FP8_TENSOR, 16, 2048, 7168, 8, 1, 8},
-    {FG_FP8_TENSOR, 1, 16384, 7168, 1, 2, 5},  {FG_FP8_TENSOR, 16, 16384, 7168, 1, 2, 5},
+    {FG_FP8_TENSOR, 1, 2048, 7168, 8, 1, 4},   {FG_FP8_TENSOR, 16, 2048, 7168, 8, 1, 4},
+    {FG_FP8_TENSOR, 1, 16384, 7168, 1, 1, 8},  {FG_FP8_TENSOR, 16, 16384, 7168, 1, 1, 8},
     {FG_FP8_BLOCK128, 1, 2048, 7168, 8, 1, 8}, {FG_FP8_BLOCK128, 16, 2048, 7168, 8, 1, 8},
     {FG_FP8_BLOCK128, 1, 16384, 7168, 1, 2, 5}, {FG_FP8_BLOCK128, 16, 16384, 7168, 1, 2, 5},
 };
 
 int64_t decode_row_limit() { return 32; }
+
+// Splits up to this many reduce inside one thread-block cluster (portable
+// cluster size); larger splits take the two-pass workspace + reduce path.
+constexpr int kMaxClusterSplit = 8;
 
 fg_status make_plan(int mode, int64_t M, int64_t N, int64_t K, int split_k, fg_plan* out) {
   memset(out, 0, sizeof *out);
@@ -150,9 +154,10 @@ fg_status make_plan(int mode, int64_t M, int64_t N, int64_t K, int split_k, fg_p
   const int64_t KB = Kb / 128;
   const int64_t tiles_n = N / 128;
   const int64_t tiles_m = (M + 15) / 16;
-  const bool large = M > decode_row_limit() && large_supported(mode);
+  // The large-M kernel has no K split; an explicit split_k > 1 keeps any M on
+  // the split-K kernel (which covers M in 16-row tiles).
+  const bool large = M > decode_row_limit() && large_supported(mode) && split_k <= 1;
   if (large) {
-    if (split_k > 1) return fail(FG_ERR_INVALID_ARG, "the large-M path takes split_k 0 or 1, got %d", split_k);
     out->path = 1;
     out->split_k = 1;
     out->tile_m = 128;
@@ -183,6 +188,16 @@ fg_status make_plan(int mode, int64_t M, int64_t N, int64_t K, int split_k, fg_p
     split = 1;
     while (split < 8 && tiles_n * tiles_m * split < want && KB / (split * 2) >= 4) split *= 2;
     if (KB / split < 8) sps = 1, stages = 8;
+  }
+  // Sweep hook: FG_DECODE_CONFIG="<slabs per stage>,<stages>" overrides the
+  // pipeline shape of every decode launch (refused when not instantiated).
+  if (const char* ov = getenv("FG_DECODE_CONFIG")) {
+    int a = 0, b = 0;
+    char tail = 0;
+    if (sscanf(ov, "%d,%d%c", &a, &b, &tail) != 2 || !decode_config_supported(DecodeConfig{mode, a, b}))
+      return fail(FG_ERR_INVALID_ARG, "FG_DECODE_CONFIG=\"%s\" is not an instantiated <slabs>,<stages> pair", ov);
+    sps = a;
+    stages = b;
   }
   if (split < 1 || split > 16) return fail(FG_ERR_INVALID_ARG, "split_k=%d outside 1..16", split);
   if (split > KB)
@@ -382,7 +397,10 @@ fg_status fg_gemm_workspace_size(int mode, int64_t M, int64_t N, int64_t K, int 
   fg_plan plan;
   fg_status s = fg_gemm_plan(mode, M, N, K, split_k, &plan);
   if (s != FG_OK) return s;
-  *bytes = plan.split_k > 1 ? static_cast<uint64_t>(plan.split_k) * M * N * 4 : 0;
+  if (plan.path == 1)
+    *bytes = (mode == FG_MXFP8 || mode == FG_MXFP4) ? sf_rows_image_bytes(mode, M, K) : 0;
+  else
+    *bytes = plan.split_k > kMaxClusterSplit ? static_cast<uint64_t>(plan.split_k) * M * N * 4 : 0;
   return FG_OK;
 }
 
@@ -409,13 +427,23 @@ fg_status fg_gemm(const void* A, const void* a_scales, int64_t M, const fg_bshuf
   if ((s = make_plan(mode, M, N, K, split_k, &plan)) != FG_OK) return s;
   const int split = plan.split_k;
   const bool defer = (flags & FG_FLAG_DEFER_REDUCE) != 0;
-  if (split > 1) {
+  const bool mx = mode == FG_MXFP8 || mode == FG_MXFP4;
+  const bool fused = plan.path == 0 && split > 1 && split <= kMaxClusterSplit && !defer;
+  if (split > 1 && !fused) {
     const uint64_t need = static_cast<uint64_t>(split) * M * N * 4;
     if (!workspace || workspace_bytes < need)
       return fail(FG_ERR_WORKSPACE, "split_k=%d needs a %llu-byte fp32 workspace", split, (unsigned long long)need);
     if (!aligned(workspace, 16)) return fail(FG_ERR_ALIGN, "workspace must be 16-byte aligned");
   } else if (defer) {
     return fail(FG_ERR_INVALID_ARG, "FG_FLAG_DEFER_REDUCE needs split_k > 1");
+  }
+  if (plan.path == 1 && mx) {
+    // the large-M MX kernel reads A's scales as 512-byte atoms relaid per call
+    const uint64_t need = sf_rows_image_bytes(mode, M, K);
+    if (!workspace || workspace_bytes < need)
+      return fail(FG_ERR_WORKSPACE, "large-M %s needs a %llu-byte workspace for the A scale image", mode_name(mode),
+                  (unsigned long long)need);
+    if (!aligned(workspace, 16)) return fail(FG_ERR_ALIGN, "workspace must be 16-byte aligned");
   }
   if ((s = check_arch()) != FG_OK) return s;
   uint32_t* err = dev_error_ptr();
@@ -442,6 +470,12 @@ fg_status fg_gemm(const void* A, const void* a_scales, int64_t M, const fg_bshuf
     p.tiles_m = static_cast<int>((M + 127) / 128);
     p.tiles_n = static_cast<int>(N / 256 + (N % 256 ? 1 : 0));
     p.debug_stall = (flags & FG_FLAG_DEBUG_STALL) ? 1 : 0;
+    if (mx) {
+      e = launch_relayout_sf_rows(mode, static_cast<const uint8_t*>(a_scales), static_cast<uint8_t*>(workspace), M, K,
+                                  st);
+      if (e != cudaSuccess) return cuda_fail(e, "A scale relayout launch");
+      p.a_sf = static_cast<const uint8_t*>(workspace);
+    }
     e = launch_large(mode, tmap, p, plan.ctas, st);
     if (e != cudaSuccess) return cuda_fail(e, "large-M kernel launch");
     return FG_OK;
@@ -462,6 +496,7 @@ fg_status fg_gemm(const void* A, const void* a_scales, int64_t M, const fg_bshuf
   p.K = static_cast<int>(K);
   p.KB = static_cast<int>(rb / 128);
   p.split = split;
+  p.fused_reduce = fused ? 1 : 0;
   p.debug_stall = (flags & FG_FLAG_DEBUG_STALL) ? 1 : 0;
   DecodeConfig cfg{mode, plan.stage_slabs, plan.stages};
   if (!decode_config_supported(cfg)) return fail(FG_ERR_INVALID_ARG, "no kernel for config %s", plan.name);
@@ -469,7 +504,7 @@ fg_status fg_gemm(const void* A, const void* a_scales, int64_t M, const fg_bshuf
   if (grid.z > 65535) return fail(FG_ERR_SHAPE, "M=%lld too large for the decode path", (long long)M);
   e = launch_decode(cfg, tmap, p, grid, st);
   if (e != cudaSuccess) return cuda_fail(e, "decode kernel launch");
-  if (split > 1 && !defer) {
+  if (split > 1 && !defer && !fused) {
     const float* as = mode == FG_FP8_TENSOR ? static_cast<const float*>(a_scales) : nullptr;
     const float* bs = mode == FG_FP8_TENSOR ? static_cast<const float*>(b->sf) : nullptr;
     e = launch_reduce(p.ws, split, M, N, as, bs, p.y, st);

@@ -12,11 +12,13 @@
 //   warp 0    producer: one bulk copy per stage for the contiguous weight
 //             slabs of the preshuffled image, one TMA tensor load per slab
 //             for the token tile (rows beyond M are zero-filled), and for MX
-//             the weight scale atoms (bulk) and token scale atoms (built by
-//             the warp's 32 lanes from the caller's E8M0 bytes);
+//             the weight scale atoms (bulk);
 //   warp 1    allocates TMEM; lane 0 issues tcgen05.cp (MX scale factors)
 //             and tcgen05.mma, and commits stage releases;
-//   warps 2-5 epilogue: TMEM -> registers -> fp32 partials (split > 1) or
+//   warps 2-5 for MX, first build the token scale atoms of each stage from
+//             the caller's E8M0 bytes (ahead of the MMA, one arrival per warp
+//             on the stage's full barrier); then
+//             epilogue: TMEM -> registers -> fp32 partials (split > 1) or
 //             scaled bf16 Y (split == 1).  For FP8_BLOCK128 they also run
 //             the per-128-K promotion: each K slab (one 128-K scale block)
 //             is multiplied into its own TMEM partial, which they read and
@@ -26,6 +28,20 @@
 //             the same per-slab partials with a weight of 1: the fold is a
 //             compensated sum, which keeps the fp32 partials of long K
 //             splits within the workspace bound.
+//
+// Split-K reduction: with split > 1 the S split CTAs of a tile run as one
+// thread-block cluster.  Each writes its fp32 partial [16 tokens][128 rows]
+// into its own shared memory; after a cluster barrier, CTA r sums rows
+// [r*128/S, (r+1)*128/S) over the S partials through distributed shared
+// memory in split order 0..S-1 (the order of the two-pass reduce, so both
+// paths give the same bits), applies the per-tensor scale and stores bf16.
+// The two-pass form (fp32 workspace + reduce kernel) remains for
+// FG_FLAG_DEFER_REDUCE and for splits beyond the cluster size limit.
+//
+// Launch order: every launch allows the next kernel of the stream to start
+// early (programmatic dependent launch).  The producer streams its first
+// stages of weights -- which no kernel writes -- before waiting for the
+// previous kernel; activations, scales and outputs are touched only after.
 //
 // MX scale factors: the block-scaled MMA reads, for row i of an operand, the
 // byte selected by the instruction's scale-factor id in TMEM lane i, column
@@ -102,7 +118,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < STAGES; ++i) {
-      mbar_init(&full_bar[i], C::APS ? 2 : 1);
+      mbar_init(&full_bar[i], C::APS ? 5 : 1);  // MX: + one arrival per scale-building warp
       mbar_init(&empty_bar[i], 1);
     }
     for (int i = 0; i < C::NBUF; ++i) {
@@ -127,9 +143,14 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = tmem_base_sh;
+  if (threadIdx.x == 0) pdl_launch_dependents();
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
+    // The first min(STAGES, niter) stages get their weight slabs (and weight
+    // scale atoms) before the wait for the previous kernel; their token tiles
+    // follow right after it.  Later stages load both together.
+    const int pre = min(STAGES, niter);
     int it = 0;
     for (; it < niter; ++it) {
       const int slot = it % STAGES;
@@ -147,41 +168,33 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_arrive_expect_tx(&full_bar[slot], bytes);
         bulk_g2s(st, p.b_img + (static_cast<size_t>(nt) * p.KB + u0 + ub) * kSlabBytes, nsl * kSlabBytes,
                  &full_bar[slot]);
-        for (int v = 0; v < nsl; ++v)
-          tma_load_2d(st + C::B_BYTES + v * kTokSlabBytes, &tmap_a, (u0 + ub + v) * 128, mt * kTokRows,
-                      &full_bar[slot]);
         if (C::APS)
           bulk_g2s(st + C::B_BYTES + C::A_BYTES,
                    p.b_sf + (static_cast<size_t>(nt) * p.KB + u0 + ub) * C::APS * 512, nsl * C::APS * 512,
                    &full_bar[slot]);
-      }
-      if (C::APS) {
-        // token scale atoms: atom t, row m -> 4 bytes (the atom's four 32-K blocks)
-        const uint8_t* asf = static_cast<const uint8_t*>(p.a_scales);
-        uint8_t* sft = st + C::B_BYTES + C::A_BYTES + C::SFW_BYTES;
-        const int natoms = nsl * C::APS;
-        for (int idx = lane; idx < natoms * kTokRows; idx += 32) {
-          const int t = idx / kTokRows, m = idx % kTokRows;
-          const int row = mt * kTokRows + m;
-          uint32_t w = 0x7F7F7F7Fu;  // 2^0 for padded rows (their values are zero)
-          if (row < p.M) {
-            const int q32 = ((u0 + ub) * C::APS + t) * 4;  // first 32-K block of the atom
-            if (MODE == kMXFP4) {
-              const uint8_t* src = asf + static_cast<size_t>(row) * (p.K / 32) + q32;
-              w = static_cast<uint32_t>(src[0]) | (static_cast<uint32_t>(src[1]) << 8) |
-                  (static_cast<uint32_t>(src[2]) << 16) | (static_cast<uint32_t>(src[3]) << 24);
-            } else {
-              const uint32_t c = asf[static_cast<size_t>(row) * (p.K / 128) + (q32 >> 2)];
-              w = c * 0x01010101u;
-            }
-          }
-          *reinterpret_cast<uint32_t*>(sft + t * 256 + m * 16) = w;
+        if (it >= pre) {
+          for (int v = 0; v < nsl; ++v)
+            tma_load_2d(st + C::B_BYTES + v * kTokSlabBytes, &tmap_a, (u0 + ub + v) * 128, mt * kTokRows,
+                        &full_bar[slot]);
         }
-        fence_proxy_async_smem();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&full_bar[slot]);
+      }
+      if (it + 1 == pre) {
+        // weights of the first stages are on their way: now wait for the
+        // previous kernel, then fetch the token tiles of those stages
+        pdl_wait();
+        if (lane == 0) {
+          for (int jt = 0; jt < pre; ++jt) {
+            const int ubj = jt * SPS;
+            const int nslj = min(SPS, nslab - ubj);
+            uint8_t* stj = smem + (jt % STAGES) * C::STAGE_BYTES;
+            for (int v = 0; v < nslj; ++v)
+              tma_load_2d(stj + C::B_BYTES + v * kTokSlabBytes, &tmap_a, (u0 + ubj + v) * 128, mt * kTokRows,
+                          &full_bar[jt % STAGES]);
+          }
+        }
       }
     }
+    if (it < pre) pdl_wait();  // aborted before the prefetch window closed
     if (lane == 0) issued_sh = it;
   } else if (warp == 1) {
     // ---------------------------------------------------------- MMA issuer
@@ -261,6 +274,49 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else {
     // ------------------------------------------------------------ epilogue
+    if (C::APS) {
+      // Before the epilogue proper, these four warps build the token scale
+      // atoms of every stage (atom t, token row m -> the 4 E8M0 bytes of the
+      // atom's four 32-K blocks), running ahead of the MMA by up to STAGES
+      // stages so the global-load latency stays hidden.
+      const uint8_t* asf = static_cast<const uint8_t*>(p.a_scales);
+      const int et = threadIdx.x - 64;  // 0..127
+      bool okb = true;
+      pdl_wait();
+      for (int it = 0; it < niter; ++it) {
+        const int slot = it % STAGES;
+        const bool w = mbar_wait(&empty_bar[slot], ((it / STAGES) & 1) ^ 1u, T, p.err, 8);
+        if (!__all_sync(0xffffffffu, w)) {
+          okb = false;
+          break;
+        }
+        const int ub = it * SPS;
+        const int nsl = min(SPS, nslab - ub);
+        uint8_t* sft = smem + slot * C::STAGE_BYTES + C::B_BYTES + C::A_BYTES + C::SFW_BYTES;
+        for (int idx = et; idx < nsl * C::APS * kTokRows; idx += 128) {
+          const int t = idx / kTokRows, m = idx % kTokRows;
+          const int row = mt * kTokRows + m;
+          uint32_t wv = 0x7F7F7F7Fu;  // 2^0 for padded rows (their values are zero)
+          if (row < p.M) {
+            const int q32 = ((u0 + ub) * C::APS + t) * 4;  // first 32-K block of the atom
+            if (MODE == kMXFP4) {
+              const uint8_t* src = asf + static_cast<size_t>(row) * (p.K / 32) + q32;
+              wv = static_cast<uint32_t>(src[0]) | (static_cast<uint32_t>(src[1]) << 8) |
+                   (static_cast<uint32_t>(src[2]) << 16) | (static_cast<uint32_t>(src[3]) << 24);
+            } else {
+              const uint32_t c = asf[static_cast<size_t>(row) * (p.K / 128) + (q32 >> 2)];
+              wv = c * 0x01010101u;
+            }
+          }
+          *reinterpret_cast<uint32_t*>(sft + t * 256 + m * 16) = wv;
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&full_bar[slot]);
+      }
+      if (!okb && lane == 0) abort_sh = 1;
+    }
+    pdl_wait();
     const int qd = warp & 3;
     const int nrow = nt * 128 + qd * 32 + lane;
     const uint32_t trow = tmem + (static_cast<uint32_t>(qd * 32) << 16);
@@ -322,6 +378,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     if (!ok) {
       if (lane == 0) abort_sh = 1;
+    } else if (p.fused_reduce) {
+      // partial [token m][local row] into this CTA's (now idle) stage memory
+      float* part = reinterpret_cast<float*>(smem);
+#pragma unroll
+      for (int m = 0; m < kTokRows; ++m) part[m * 128 + qd * 32 + lane] = acc[m];
     } else if (p.split > 1) {
 #pragma unroll
       for (int m = 0; m < kTokRows; ++m) {
@@ -342,6 +403,38 @@ __global__ void __launch_bounds__(kThreads, 1)
   // ------------------------------------------------------------- teardown
   tc_fence_before();
   __syncthreads();
+  if (p.fused_reduce) {
+    // Every thread of every CTA of the cluster passes both barriers, on the
+    // normal and on the abort path alike.
+    cluster_sync();  // all partials of the tile are in place
+    const int et = static_cast<int>(threadIdx.x) - 64;
+    if (!abort_sh && et >= 0) {
+      const int S = p.split;
+      const int R = 128 / S;          // rows this CTA reduces
+      const int r0 = split * R;
+      float scale = 1.f;
+      if (MODE == kTensor) scale = __ldg(static_cast<const float*>(p.a_scales)) * __ldg(p.b_s);
+      const float* part = reinterpret_cast<const float*>(smem);
+      for (int e = et; e < kTokRows * R / 4; e += 128) {
+        const int m = e / (R / 4);
+        const int lr = r0 + (e % (R / 4)) * 4;
+        const int row = mt * kTokRows + m;
+        if (row >= p.M) continue;
+        float4 a = ld_dsmem_f32x4(part + m * 128 + lr, 0);
+        for (int s2 = 1; s2 < S; ++s2) {
+          const float4 v = ld_dsmem_f32x4(part + m * 128 + lr, s2);
+          a.x += v.x; a.y += v.y; a.z += v.z; a.w += v.w;
+        }
+        const __nv_bfloat162 lo = __floats2bfloat162_rn(a.x * scale, a.y * scale);
+        const __nv_bfloat162 hi = __floats2bfloat162_rn(a.z * scale, a.w * scale);
+        uint2 o;
+        o.x = *reinterpret_cast<const uint32_t*>(&lo);
+        o.y = *reinterpret_cast<const uint32_t*>(&hi);
+        *reinterpret_cast<uint2*>(p.y + static_cast<size_t>(row) * p.N + nt * 128 + lr) = o;
+      }
+    }
+    cluster_sync();  // no CTA leaves while a peer may still read its partial
+  }
   if (abort_sh) {
     // Let every copy this CTA started land before its shared memory goes
     // away, and every MMA it issued finish before TMEM is released.
@@ -365,20 +458,42 @@ cudaError_t launch_one(const CUtensorMap& tmap_a, const DecodeParams& p, dim3 gr
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
-  decode_kernel<MODE, SPS, STAGES><<<grid, kThreads, C::SMEM, stream>>>(tmap_a, p);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = C::SMEM;
+  cfg.stream = stream;
+  cudaLaunchAttribute attrs[2];
+  int na = 0;
+  attrs[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attrs[na].val.programmaticStreamSerializationAllowed = 1;
+  ++na;
+  if (p.fused_reduce) {
+    attrs[na].id = cudaLaunchAttributeClusterDimension;
+    attrs[na].val.clusterDim.x = 1;
+    attrs[na].val.clusterDim.y = static_cast<unsigned>(p.split);
+    attrs[na].val.clusterDim.z = 1;
+    ++na;
+  }
+  cfg.attrs = attrs;
+  cfg.numAttrs = na;
+  return cudaLaunchKernelEx(&cfg, decode_kernel<MODE, SPS, STAGES>, tmap_a, p);
 }
 
 // Instantiated configurations: (slabs per stage, stages).
 #define FG_DECODE_CONFIGS(X, MODE) \
+  X(MODE, 1, 4)                    \
   X(MODE, 1, 8)                    \
-  X(MODE, 2, 5)
+  X(MODE, 2, 3)                    \
+  X(MODE, 2, 5)                    \
+  X(MODE, 4, 2)
 
 }  // namespace
 
 bool decode_config_supported(const DecodeConfig& c) {
   if (c.mode < kBF16 || c.mode > kMXFP4) return false;
-  return (c.sps == 1 && c.stages == 8) || (c.sps == 2 && c.stages == 5);
+  return (c.sps == 1 && (c.stages == 4 || c.stages == 8)) || (c.sps == 2 && (c.stages == 3 || c.stages == 5)) ||
+         (c.sps == 4 && c.stages == 2);
 }
 
 cudaError_t launch_decode(const DecodeConfig& c, const CUtensorMap& tmap_a, const DecodeParams& p, dim3 grid,

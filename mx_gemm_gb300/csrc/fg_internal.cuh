@@ -29,6 +29,7 @@ struct DecodeParams {
   int M, N, K;
   int KB;                  // 128-byte slabs per row
   int split;
+  int fused_reduce;        // split > 1: the split CTAs of a tile form a cluster and reduce in DSMEM
   int debug_stall;
 };
 
@@ -42,6 +43,7 @@ struct DecodeConfig {
 struct LargeParams {
   const uint8_t* b_img;
   const uint8_t* b_sf;     // MX weight scale image
+  const uint8_t* a_sf;     // MX activation scale image (atoms per 128-row tile of A)
   const float* b_s;        // FP8_TENSOR scalar
   const void* a_scales;    // FP8_TENSOR scalar / MX E8M0 [M][K/blk]
   __nv_bfloat16* y;
@@ -54,6 +56,9 @@ struct LargeParams {
 };
 
 bool decode_config_supported(const DecodeConfig& c);
+// Kernels are launched with programmatic dependent launch (they may start
+// while the previous kernel of the stream finishes; they wait for it before
+// touching anything it could write or read).
 cudaError_t launch_decode(const DecodeConfig& cfg, const CUtensorMap& tmap_a, const DecodeParams& p, dim3 grid,
                           cudaStream_t stream);
 
@@ -64,6 +69,9 @@ cudaError_t launch_relayout_b(const uint8_t* src, uint8_t* dst, int64_t N, int64
                               cudaStream_t stream);
 cudaError_t launch_relayout_sf(int mode, const uint8_t* src, uint8_t* dst, int64_t N, int64_t K, bool inverse,
                                cudaStream_t stream);
+uint64_t sf_rows_image_bytes(int mode, int64_t rows, int64_t K);
+cudaError_t launch_relayout_sf_rows(int mode, const uint8_t* src, uint8_t* dst, int64_t rows, int64_t K,
+                                    cudaStream_t stream);
 cudaError_t launch_reduce(const float* ws, int split, int64_t M, int64_t N, const float* a_s, const float* b_s,
                           __nv_bfloat16* y, cudaStream_t stream);
 

@@ -244,13 +244,235 @@ cudaError_t launch_mode(const CUtensorMap& tmap_a, const LargeParams& p, int cta
   return cudaGetLastError();
 }
 
+
+// ------------------------------------------------------------------ MX form
+//
+// Block-scaled variant (mxfp8: kind::mxf8f6f4, one E8M0 per 32 K of the
+// hardware block -- the 128-K mxfp8 scale repeated four times in the atoms;
+// mxfp4: kind::mxf4 with two E8M0 per 64-K MMA).  Per stage the producer
+// also bulk-copies the scale atoms of the A tile (from the per-call A scale
+// image) and of the two weight slabs; the MMA thread moves them into a TMEM
+// ring with tcgen05.cp before the stage's MMAs.  TMEM holds one 256-column
+// accumulator plus that ring, so the epilogue runs on eight warps that each
+// pull their 128 columns into registers and release the accumulator before
+// converting and storing -- the next tile's MMAs overlap the stores.
+constexpr int kMxThreads = 320;
+
+template <int MODE>
+struct MxCfg {
+  static constexpr int APS = MODE == kMXFP4 ? 2 : 1;  // atoms per slab (4 K-blocks of 32 each)
+  static constexpr int SFA_BYTES = APS * 512;
+  static constexpr int SFB_BYTES = 2 * APS * 512;
+  static constexpr int STAGE_RAW = kABytes + kBBytes + SFA_BYTES + SFB_BYTES;
+  static constexpr int STAGE_BYTES = (STAGE_RAW + 1023) / 1024 * 1024;
+  static constexpr int SMEM = kStages * STAGE_BYTES + 1024;
+  static constexpr int SF_COLS = APS * 4 + APS * 8;  // TMEM columns per stage: A (128 rows) + B (256 rows)
+  static_assert(SMEM <= 232448, "shared memory budget");
+  static_assert(256 + kStages * SF_COLS <= kTmemCols, "TMEM budget");
+};
+
+template <int MODE>
+__global__ void __launch_bounds__(kMxThreads, 1)
+    large_mx_kernel(const __grid_constant__ CUtensorMap tmap_a, const LargeParams p) {
+  using C = MxCfg<MODE>;
+  extern __shared__ uint8_t dsmem[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(dsmem) + 1023) & ~uintptr_t(1023));
+  __shared__ __align__(8) uint64_t full_bar[kStages];
+  __shared__ __align__(8) uint64_t empty_bar[kStages];
+  __shared__ __align__(8) uint64_t accf_bar, acce_bar, stall_bar, drain_bar;
+  __shared__ uint32_t tmem_base_sh;
+  __shared__ int abort_sh, issued_sh, consumed_sh, mma_any_sh;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int tiles = p.tiles_m * p.tiles_n;
+  const int KB = p.KB;
+  const uint64_t T = p.timeout_ns;
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < kStages; ++i) {
+      mbar_init(&full_bar[i], 1);
+      mbar_init(&empty_bar[i], 1);
+    }
+    mbar_init(&accf_bar, 1);
+    mbar_init(&acce_bar, 8);
+    mbar_init(&stall_bar, 1);
+    mbar_init(&drain_bar, 1);
+    abort_sh = 0;
+    issued_sh = 0;
+    consumed_sh = 0;
+    mma_any_sh = 0;
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(&tmem_base_sh, kTmemCols);
+    tmem_relinquish();
+  }
+  if (warp == 0 && lane == 0) prefetch_tmap(&tmap_a);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = tmem_base_sh;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      int it = 0;
+      bool ok = true;
+      for (int t = blockIdx.x; ok && t < tiles; t += gridDim.x) {
+        const TileCoord tc = tile_coord(t, p.tiles_m, p.tiles_n);
+        const int nslabs_n = min(2, p.N / 128 - 2 * tc.n);
+        for (int kb = 0; kb < KB; ++kb, ++it) {
+          const int slot = it % kStages;
+          if (!mbar_wait(&empty_bar[slot], ((it / kStages) & 1) ^ 1u, T, p.err, 21)) {
+            ok = false;
+            break;
+          }
+          uint8_t* st = smem + slot * C::STAGE_BYTES;
+          mbar_arrive_expect_tx(&full_bar[slot], kABytes + C::SFA_BYTES + nslabs_n * (16384 + C::APS * 512));
+          tma_load_2d(st, &tmap_a, kb * 128, tc.m * kBM, &full_bar[slot]);
+          bulk_g2s(st + kABytes + kBBytes, p.a_sf + (static_cast<size_t>(tc.m) * KB + kb) * C::SFA_BYTES,
+                   C::SFA_BYTES, &full_bar[slot]);
+          for (int h = 0; h < nslabs_n; ++h) {
+            const size_t slab = static_cast<size_t>(2 * tc.n + h) * KB + kb;
+            bulk_g2s(st + kABytes + h * 16384, p.b_img + slab * 16384, 16384, &full_bar[slot]);
+            bulk_g2s(st + kABytes + kBBytes + C::SFA_BYTES + h * C::APS * 512, p.b_sf + slab * C::APS * 512,
+                     C::APS * 512, &full_bar[slot]);
+          }
+        }
+      }
+      issued_sh = it;
+      if (!ok) abort_sh = 1;
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      bool ok = true;
+      if (p.debug_stall) ok = mbar_wait(&stall_bar, 0, T, p.err, 22);
+      int it = 0, ti = 0;
+      for (int t = blockIdx.x; ok && t < tiles; t += gridDim.x, ++ti) {
+        if (!mbar_wait(&acce_bar, (ti & 1) ^ 1u, T, p.err, 23)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        for (int kb = 0; kb < KB; ++kb, ++it) {
+          const int slot = it % kStages;
+          if (!mbar_wait(&full_bar[slot], (it / kStages) & 1, T, p.err, 24)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          mma_any_sh = 1;
+          uint8_t* st = smem + slot * C::STAGE_BYTES;
+          const uint32_t sfa = 256 + slot * C::SF_COLS;
+          const uint32_t sfb = sfa + C::APS * 4;
+          uint8_t* sfa_sm = st + kABytes + kBBytes;
+          uint8_t* sfb_sm = sfa_sm + C::SFA_BYTES;
+#pragma unroll
+          for (int g = 0; g < C::APS; ++g) {
+            tc_cp_32x128b_warpx4(tmem + sfa + 4 * g, sdesc_plain_rows16(smem_u32(sfa_sm + 512 * g)));
+            tc_cp_32x128b_warpx4(tmem + sfb + 8 * g, sdesc_plain_rows16(smem_u32(sfb_sm + 512 * g)));
+            tc_cp_32x128b_warpx4(tmem + sfb + 8 * g + 4,
+                                 sdesc_plain_rows16(smem_u32(sfb_sm + C::APS * 512 + 512 * g)));
+          }
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            const uint64_t adesc = sdesc_sw128(smem_u32(st + j * 32));
+            const uint64_t bdesc = sdesc_sw128(smem_u32(st + kABytes + j * 32));
+            if (MODE == kMXFP8) {
+              mma_mxf8f6f4(tmem, adesc, bdesc, idesc_mx(kBM, kBN, 0u, j, j), tmem + sfa, tmem + sfb, (kb | j) != 0);
+            } else {
+              const int g = j >> 1, id = 2 * (j & 1);
+              mma_mxf4(tmem, adesc, bdesc, idesc_mx(kBM, kBN, 1u, id, id), tmem + sfa + 4 * g, tmem + sfb + 8 * g,
+                       (kb | j) != 0);
+            }
+          }
+          tc_commit(&empty_bar[slot]);
+        }
+        if (!ok) {
+          ++it;
+          break;
+        }
+        tc_commit(&accf_bar);
+      }
+      consumed_sh = it;
+      if (!ok) abort_sh = 1;
+      if (mma_any_sh) {
+        tc_commit(&drain_bar);
+        mbar_wait(&drain_bar, 0, T, p.err, 25);
+      }
+    }
+  } else {
+    // eight epilogue warps: lane quarter warp % 4, column half (warp - 2) / 4
+    const int qd = warp & 3;
+    const int half = (warp - 2) >> 2;
+    int ti = 0;
+    for (int t = blockIdx.x; t < tiles; t += gridDim.x, ++ti) {
+      const bool w = mbar_wait(&accf_bar, ti & 1, T, p.err, 26);
+      if (!__all_sync(0xffffffffu, w)) {
+        if (lane == 0) abort_sh = 1;
+        break;
+      }
+      tc_fence_after();
+      uint32_t v[128];
+      const uint32_t taddr = tmem + half * 128 + (static_cast<uint32_t>(qd * 32) << 16);
+      tmem_ld32(taddr + 0, *reinterpret_cast<uint32_t(*)[32]>(&v[0]));
+      tmem_ld32(taddr + 32, *reinterpret_cast<uint32_t(*)[32]>(&v[32]));
+      tmem_ld32(taddr + 64, *reinterpret_cast<uint32_t(*)[32]>(&v[64]));
+      tmem_ld32(taddr + 96, *reinterpret_cast<uint32_t(*)[32]>(&v[96]));
+      tmem_wait_ld();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&acce_bar);  // accumulator free: the next tile may start
+      const TileCoord tc = tile_coord(t, p.tiles_m, p.tiles_n);
+      const int row = tc.m * kBM + qd * 32 + lane;
+      const int col0 = tc.n * kBN + half * 128;
+      if (row < p.M && col0 < p.N) {
+        uint4* dst = reinterpret_cast<uint4*>(p.y + static_cast<size_t>(row) * p.N + col0);
+#pragma unroll
+        for (int q = 0; q < 16; ++q) {
+          uint4 o;
+          o.x = pack_bf16x2(__uint_as_float(v[8 * q + 0]), __uint_as_float(v[8 * q + 1]));
+          o.y = pack_bf16x2(__uint_as_float(v[8 * q + 2]), __uint_as_float(v[8 * q + 3]));
+          o.z = pack_bf16x2(__uint_as_float(v[8 * q + 4]), __uint_as_float(v[8 * q + 5]));
+          o.w = pack_bf16x2(__uint_as_float(v[8 * q + 6]), __uint_as_float(v[8 * q + 7]));
+          dst[q] = o;
+        }
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (abort_sh && threadIdx.x == 0) {
+    for (int it = consumed_sh; it < issued_sh; ++it)
+      mbar_wait(&full_bar[it % kStages], (it / kStages) & 1, T, nullptr, 0);
+  }
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 1) tmem_dealloc(tmem, kTmemCols);
+}
+
+template <int MODE>
+cudaError_t launch_mx(const CUtensorMap& tmap_a, const LargeParams& p, int ctas, cudaStream_t stream) {
+  static bool attr_set = false;
+  if (!attr_set) {
+    cudaError_t e = cudaFuncSetAttribute(large_mx_kernel<MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         MxCfg<MODE>::SMEM);
+    if (e != cudaSuccess) return e;
+    attr_set = true;
+  }
+  large_mx_kernel<MODE><<<ctas, kMxThreads, MxCfg<MODE>::SMEM, stream>>>(tmap_a, p);
+  return cudaGetLastError();
+}
+
 }  // namespace
 
-bool large_supported(int mode) { return mode == kBF16 || mode == kTensor; }
+bool large_supported(int mode) { return mode == kBF16 || mode == kTensor || mode == kMXFP8 || mode == kMXFP4; }
 
 cudaError_t launch_large(int mode, const CUtensorMap& tmap_a, const LargeParams& p, int ctas, cudaStream_t stream) {
   if (mode == kBF16) return launch_mode<kBF16>(tmap_a, p, ctas, stream);
   if (mode == kTensor) return launch_mode<kTensor>(tmap_a, p, ctas, stream);
+  if (mode == kMXFP8) return launch_mx<kMXFP8>(tmap_a, p, ctas, stream);
+  if (mode == kMXFP4) return launch_mx<kMXFP4>(tmap_a, p, ctas, stream);
   return cudaErrorNotSupported;
 }
 

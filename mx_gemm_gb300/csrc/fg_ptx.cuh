@@ -245,6 +245,38 @@ __device__ __forceinline__ void tmem_st4(uint32_t taddr, uint32_t a, uint32_t b,
 
 __device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
+// ------------------------------------------------- clusters and launch order
+
+// Every thread of every CTA of the cluster must execute this, the same number
+// of times; the library's kernels only call it on paths all threads take.
+__device__ __forceinline__ void cluster_sync() {
+  asm volatile(
+      "barrier.cluster.arrive.release.aligned;\n"
+      "barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+// Load 4 floats from the shared memory of CTA `rank` of this cluster, at the
+// offset `local` has in this CTA's shared memory.
+__device__ __forceinline__ float4 ld_dsmem_f32x4(const void* local, uint32_t rank) {
+  uint32_t remote;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(smem_u32(local)), "r"(rank));
+  float4 v;
+  asm volatile("ld.shared::cluster.v4.f32 {%0,%1,%2,%3}, [%4];"
+               : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+               : "r"(remote)
+               : "memory");
+  return v;
+}
+
+// Programmatic dependent launch: let the next kernel of the stream start its
+// CTAs, and wait until the previous kernel has finished and its writes are
+// visible.  Both are no-ops for a launch without the attribute.
+__device__ __forceinline__ void pdl_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 // ------------------------------------------------------------- descriptors
 
 // Shared-memory matrix descriptor for a K-major operand stored in the

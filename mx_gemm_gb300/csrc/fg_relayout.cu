@@ -13,6 +13,7 @@
 #include <cuda_bf16.h>
 
 #include "fg_internal.cuh"
+#include "fg_ptx.cuh"
 
 namespace fg {
 
@@ -73,33 +74,76 @@ __global__ void relayout_sf_kernel(const uint8_t* __restrict__ src, uint8_t* __r
   }
 }
 
+// Activation scales of the MX modes, [rows][K/blk] E8M0 bytes, into the same
+// 512-byte atoms as the weight image, per 128-row tile of A; rows past the
+// end read as 2^0 (their A values are zero-filled by the tile loads).
+__global__ void relayout_sf_rows_kernel(const uint8_t* __restrict__ src, uint8_t* __restrict__ dst, int64_t rows,
+                                        int64_t K, int mode) {
+  const int aps = mode == kMXFP4 ? 2 : 1;
+  const int64_t KB = mode == kMXFP4 ? K / 256 : K / 128;
+  const int64_t sf_cols = mode == kMXFP4 ? K / 32 : K / 128;
+  const int64_t total = ((rows + 127) / 128) * KB * aps * 512;
+  for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < total;
+       i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const int64_t atom = i >> 9;
+    const int off = static_cast<int>(i & 511);
+    const int r = (off >> 4) + 32 * ((off & 15) >> 2);
+    const int j = off & 3;
+    const int64_t mb = atom / (KB * aps);
+    const int64_t q32 = (atom - mb * KB * aps) * 4 + j;
+    const int64_t m = mb * 128 + r;
+    const int64_t col = mode == kMXFP4 ? q32 : (q32 >> 2);
+    dst[i] = m < rows ? __ldg(src + m * sf_cols + col) : uint8_t(127);
+  }
+}
+
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   const __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
   return *reinterpret_cast<const uint32_t*>(&v);
 }
 
 // Y[i] = bf16_rne(scale * sum_s ws[s][i]) over the flattened M*N outputs,
-// eight consecutive outputs per thread (two 16-byte loads per split, one
-// 16-byte store).
-__global__ void reduce_kernel(const float4* __restrict__ ws, int split, int64_t mn8, const float* __restrict__ a_s,
-                              const float* __restrict__ b_s, uint4* __restrict__ y) {
+// four consecutive outputs per thread.  All S partial loads of a thread are
+// issued before the first add (S is a template constant), so the kernel
+// costs one memory round trip instead of S; the adds then run in split
+// order.
+template <int S>
+__global__ void reduce_kernel(const float4* __restrict__ ws, int64_t mn4, const float* __restrict__ a_s,
+                              const float* __restrict__ b_s, uint2* __restrict__ y) {
+  pdl_wait();  // the partials come from the kernel before this one
+  pdl_launch_dependents();
   const float scale = (a_s != nullptr) ? __ldg(a_s) * __ldg(b_s) : 1.0f;
-  const int64_t mn4 = mn8 * 2;
-  for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < mn8;
+  for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < mn4;
        i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
-    float4 a = __ldcs(ws + 2 * i), b = __ldcs(ws + 2 * i + 1);
-    for (int s = 1; s < split; ++s) {
-      const float4 c = __ldcs(ws + s * mn4 + 2 * i), d = __ldcs(ws + s * mn4 + 2 * i + 1);
-      a.x += c.x; a.y += c.y; a.z += c.z; a.w += c.w;
-      b.x += d.x; b.y += d.y; b.z += d.z; b.w += d.w;
+    float4 v[S];
+#pragma unroll
+    for (int s = 0; s < S; ++s) v[s] = __ldcs(ws + s * mn4 + i);
+    float4 a = v[0];
+#pragma unroll
+    for (int s = 1; s < S; ++s) {
+      a.x += v[s].x; a.y += v[s].y; a.z += v[s].z; a.w += v[s].w;
     }
-    uint4 o;
+    uint2 o;
     o.x = pack_bf16x2(a.x * scale, a.y * scale);
     o.y = pack_bf16x2(a.z * scale, a.w * scale);
-    o.z = pack_bf16x2(b.x * scale, b.y * scale);
-    o.w = pack_bf16x2(b.z * scale, b.w * scale);
     y[i] = o;
   }
+}
+
+template <int S>
+cudaError_t launch_reduce_s(const float* ws, int64_t mn4, const float* a_s, const float* b_s, __nv_bfloat16* y,
+                            cudaStream_t stream) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid_for(mn4, 128));
+  cfg.blockDim = dim3(128);
+  cfg.stream = stream;
+  cudaLaunchAttribute attr;
+  attr.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr.val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = &attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, reduce_kernel<S>, reinterpret_cast<const float4*>(ws), mn4, a_s, b_s,
+                            reinterpret_cast<uint2*>(y));
 }
 
 }  // namespace
@@ -123,13 +167,32 @@ cudaError_t launch_relayout_sf(int mode, const uint8_t* src, uint8_t* dst, int64
   return cudaGetLastError();
 }
 
+uint64_t sf_rows_image_bytes(int mode, int64_t rows, int64_t K) {
+  const int aps = mode == kMXFP4 ? 2 : 1;
+  const int64_t KB = mode == kMXFP4 ? K / 256 : K / 128;
+  return static_cast<uint64_t>((rows + 127) / 128) * KB * aps * 512;
+}
+
+cudaError_t launch_relayout_sf_rows(int mode, const uint8_t* src, uint8_t* dst, int64_t rows, int64_t K,
+                                    cudaStream_t stream) {
+  const int64_t work = static_cast<int64_t>(sf_rows_image_bytes(mode, rows, K));
+  if (work == 0) return cudaSuccess;
+  relayout_sf_rows_kernel<<<grid_for(work, 256), 256, 0, stream>>>(src, dst, rows, K, mode);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_reduce(const float* ws, int split, int64_t M, int64_t N, const float* a_s, const float* b_s,
                           __nv_bfloat16* y, cudaStream_t stream) {
-  const int64_t mn8 = M * N / 8;
-  if (mn8 == 0) return cudaSuccess;
-  reduce_kernel<<<grid_for(mn8, 256), 256, 0, stream>>>(reinterpret_cast<const float4*>(ws), split, mn8, a_s, b_s,
-                                                        reinterpret_cast<uint4*>(y));
-  return cudaGetLastError();
+  const int64_t mn4 = M * N / 4;
+  if (mn4 == 0) return cudaSuccess;
+  switch (split) {
+#define FG_RED(S_) \
+  case S_: return launch_reduce_s<S_>(ws, mn4, a_s, b_s, y, stream);
+    FG_RED(1) FG_RED(2) FG_RED(3) FG_RED(4) FG_RED(5) FG_RED(6) FG_RED(7) FG_RED(8)
+    FG_RED(9) FG_RED(10) FG_RED(11) FG_RED(12) FG_RED(13) FG_RED(14) FG_RED(15) FG_RED(16)
+#undef FG_RED
+    default: return cudaErrorInvalidValue;
+  }
 }
 
 }  // namespace fg

@@ -91,8 +91,12 @@ def test_plan_heuristic_and_table(fg):
     assert e.value.status == fg.FG_ERR_SHAPE
     with pytest.raises(fg.FgError):
         fg.gemm_plan("fp8_tensor", 1, 256, 7168, split_k=17)
-    assert fg.gemm_workspace_size("fp8_tensor", 1, 2048, 7168, 4) == 4 * 2048 * 4
+    # splits up to 8 reduce inside a cluster (no workspace); larger ones need one
+    assert fg.gemm_workspace_size("fp8_tensor", 1, 2048, 7168, 4) == 0
+    assert fg.gemm_workspace_size("fp8_tensor", 3, 2048, 7168, 16) == 16 * 3 * 2048 * 4
     assert fg.gemm_workspace_size("fp8_tensor", 1, 16384, 7168, 1) == 0
+    # large-M MX needs room for the per-call A scale image
+    assert fg.gemm_workspace_size("mxfp4", 4096, 16384, 7168) == 32 * 28 * 2 * 512
 
 
 def _fake_desc(fg, mode=1, N=128, K=128):
@@ -163,3 +167,14 @@ def test_product_path_has_no_oracle_dependency():
                 text = open(os.path.join(dirpath, f)).read()
                 assert "import oracle" not in text and "from oracle" not in text, f
                 assert "orc_" not in text, f
+
+
+def test_decode_config_override_is_validated(fg, monkeypatch):
+    monkeypatch.setenv("FG_DECODE_CONFIG", "1,4")
+    p = fg.gemm_plan("fp8_tensor", 1, 2048, 7168)
+    assert (p["stage_slabs"], p["stages"]) == (1, 4)
+    for bad in ("3,3", "1", "x,y", "1,4,5", "2,5z"):
+        monkeypatch.setenv("FG_DECODE_CONFIG", bad)
+        with pytest.raises(fg.FgError) as e:
+            fg.gemm_plan("fp8_tensor", 1, 2048, 7168)
+        assert e.value.status == fg.FG_ERR_INVALID_ARG

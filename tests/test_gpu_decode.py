@@ -43,7 +43,7 @@ def test_split_outputs_agree(mode):
     M, N, K = 4, 256, 2048
     c = Case(mode, *inputs.operands(mode, M, N, K, 1, 2, 3))
     y1 = y_to_f64(c.gemm(split_k=1))
-    for S in (2, 4, 8):
+    for S in (2, 4, 8, 16):   # 2..8 reduce in a cluster, 16 through the workspace + reduce kernel
         if S > _slabs(mode, K):
             continue
         yS = y_to_f64(c.gemm(split_k=S))
@@ -51,8 +51,11 @@ def test_split_outputs_agree(mode):
 
 
 @pytest.mark.parametrize("mode", MODES)
-def test_deferred_reduce_equals_fused_call(mode):
-    M, N, K, S = 16, 256, 2048, 4
+@pytest.mark.parametrize("S", [2, 4, 8])
+def test_deferred_reduce_equals_fused_call(mode, S):
+    """Two-pass (fp32 workspace + reduce kernel) and the in-cluster reduce sum
+    the same partials in the same order: identical bits."""
+    M, N, K = 16, 256, 2048
     c = Case(mode, *inputs.operands(mode, M, N, K, 9, 10, 11))
     ws = torch.empty(S * M * N, dtype=torch.float32, device="cuda")
     c.gemm(split_k=S, flags=fg.FG_FLAG_DEFER_REDUCE, workspace=ws)
@@ -159,8 +162,9 @@ def test_error_paths_on_device():
     with pytest.raises(fg.FgError) as e:
         fg.gemm(c.dA, c.pb, c.da_s, mode="mxfp8", Y=Y)
     assert e.value.status == fg.FG_ERR_LAYOUT
-    with pytest.raises(fg.FgError) as e:
-        fg.gemm(c.dA, c.pb, c.da_s, split_k=4, Y=Y, workspace=torch.empty(8, device="cuda"))
+    with pytest.raises(fg.FgError) as e:     # deferred partials need split*M*N*4 bytes
+        fg.gemm(c.dA, c.pb, c.da_s, split_k=4, Y=Y, workspace=torch.empty(8, device="cuda"),
+                flags=fg.FG_FLAG_DEFER_REDUCE)
     assert e.value.status == fg.FG_ERR_WORKSPACE
     buf = torch.zeros(M * K + 16, dtype=torch.uint8, device="cuda")
     with pytest.raises(fg.FgError) as e:

@@ -1,8 +1,10 @@
-"""Parity of the large-M GEMM (bf16 and fp8 per-tensor) with the oracle.
+"""Parity of the large-M GEMM (bf16, fp8 per-tensor, mxfp8, mxfp4) with the
+oracle.
 
 Small shapes compare every output (ragged M tiles, a half-empty last weight
-tile); the pages' shapes (bf16 54560x8192x8192, fp8 4096x4096x8192) run in
-the dispatch configuration the bench times and compare 256 seeded full rows.
+tile); the pages' shapes (bf16 54560x8192x8192, fp8 4096x4096x8192, MX
+4096x16384x7168) run in the dispatch configuration the bench times and
+compare 256 seeded full rows.
 """
 import numpy as np
 import pytest
@@ -17,7 +19,7 @@ from tests.gpu_util import Case, y_to_f64
 pytestmark = pytest.mark.gpu
 
 
-@pytest.mark.parametrize("mode", ["bf16", "fp8_tensor"])
+@pytest.mark.parametrize("mode", ["bf16", "fp8_tensor", "mxfp8", "mxfp4"])
 @pytest.mark.parametrize("M,N,K", [(33, 256, 512), (129, 384, 1024), (300, 512, 2048), (1000, 1280, 1536)])
 def test_large_small_shapes(mode, M, N, K):
     c = Case(mode, *inputs.operands(mode, M, N, K, 10 + M, 20 + N, 30 + K))
@@ -26,26 +28,34 @@ def test_large_small_shapes(mode, M, N, K):
     parity.assert_y_close(y_to_f64(c.gemm()), c.ref(), f"{mode} {M}x{N}x{K}")
 
 
-@pytest.mark.parametrize("mode", ["bf16", "fp8_tensor"])
+@pytest.mark.parametrize("mode", ["bf16", "fp8_tensor", "mxfp8", "mxfp4"])
 def test_large_identity_is_bit_exact(mode):
     M, N, K = 300, 512, 1024
-    _, B, _, _ = inputs.operands(mode, 1, N, K, 3, 4, 5)
+    _, B, _, b_s = inputs.operands(mode, 1, N, K, 3, 4, 5)
     A = np.zeros((M, K), np.uint16 if mode == "bf16" else np.uint8)
-    one = 0x3F80 if mode == "bf16" else 0x38
+    one = {"bf16": 0x3F80, "mxfp4": 0x2}.get(mode, 0x38)
     for m in range(M):
         A[m, (3 * m + 1) % K] = one
-    a_s = b_s = None
+    a_s = None
     if mode == "fp8_tensor":
         a_s, b_s = np.array([1.0], np.float32), np.array([1.0], np.float32)
+    elif mode == "mxfp8":
+        a_s = np.full((M, K // 128), 127, np.uint8)
+    elif mode == "mxfp4":
+        A = inputs.pack_e2m1(A)
+        a_s = np.full((M, K // 32), 127, np.uint8)
     c = Case(mode, A, B, a_s, b_s)
     ref = c.ref()
     assert np.array_equal(y_to_f64(c.gemm()), parity.bf16_bits_to_f64(oracle.round_bf16(ref)))
 
 
-@pytest.mark.parametrize("mode,M,N,K", [("fp8_tensor", 4096, 4096, 8192), ("bf16", 54560, 8192, 8192)])
-def test_large_workload_parity_sampled_rows(mode, M, N, K):
-    name = "large_bf16_54560x8192x8192_fp8_4096x4096x8192"
-    idx = 0 if mode == "bf16" else 1
+@pytest.mark.parametrize("mode,M,N,K,name,idx", [
+    ("fp8_tensor", 4096, 4096, 8192, "large_bf16_54560x8192x8192_fp8_4096x4096x8192", 1),
+    ("bf16", 54560, 8192, 8192, "large_bf16_54560x8192x8192_fp8_4096x4096x8192", 0),
+    ("mxfp8", 4096, 16384, 7168, "mx_mxfp8_mxfp4_n16384_k7168", 2),
+    ("mxfp4", 4096, 16384, 7168, "mx_mxfp8_mxfp4_n16384_k7168", 5),
+])
+def test_large_workload_parity_sampled_rows(mode, M, N, K, name, idx):
     A, B, a_s, b_s = inputs.workload_operands(name, idx)
     c = Case(mode, A, B, a_s, b_s)
     Y = c.gemm()
