@@ -302,9 +302,13 @@ def main():
     # operands: `rotate` copies of every activation and preshuffled weight
     host_ops = host_ops_fn()
     cases = []
+    l2_bytes = torch.cuda.get_device_properties(dev).L2_cache_size
     for c, (A, B, a_s, b_s) in zip(wl["cases"], host_ops):
         dB, db_s = to_dev(B), to_dev(b_s)
-        R = max(1, args.rotate)
+        # enough weight copies that a case timed on its own cycles through
+        # more than twice the L2 (a small weight would stay resident otherwise)
+        wb = c["N"] * c["K"] * elem_bytes(c["mode"])
+        R = max(1, args.rotate, -(-2 * l2_bytes // int(wb)) if kind == "decode" else 1)
         pbs = [fg.preshuffle_b(c["mode"], dB, db_s, K=c["K"]) for _ in range(R)]
         del dB
         dA0 = to_dev(A)
@@ -458,9 +462,10 @@ def main():
             "scaling": "weak", "vs_baseline": None, "dtype": dtype, "data": "synthetic",
             "config": {"workload": args.workload,
                        "shapes": [[x["c"]["M"], x["c"]["N"], x["c"]["K"]] for x in cases],
-                       "l2": "inputs larger than L2: %d rotating copies, %.0f MB of operands cycled per %d steps"
-                             % (args.rotate, args.rotate * (wbytes + (abytes if kind == "large" else 0)) / 1e6,
-                                args.rotate),
+                       "l2": "inputs larger than L2: every case cycles through copies of its operands "
+                             "(%s copies) so that more than twice the L2 (%d MB) passes between reuses; "
+                             "%.0f MB of weights per step" % ("/".join(str(len(x["pbs"])) for x in cases),
+                                                              l2_bytes // 10**6, wbytes / 1e6),
                        "parallelism": "replicas" if world > 1 else "single"},
             "per_case": per_case,
             "roofline": {"bound": bound, "achieved": round(achieved, 1), "peak": peak, "unit": unit,

@@ -133,13 +133,19 @@ struct TableRow {
   int split, sps, stages;
 };
 
-// Exact-shape rows (decode shapes measured on this part); anything else
-// falls through to the heuristic below.
+// Exact-shape rows: the decode shapes of the split-K page (K=7168), each
+// the fastest (split, slabs per stage, stages) of a sweep on GB300 (whole
+// four-GEMM step for the fp8 modes, per shape for MX).  Anything else falls
+// through to the heuristic below.
 const TableRow kTable[] = {
-    {FG_FP8_TENSOR, 1, 2048, 7168, 8, 1, 4},   {FG_FP8_TENSOR, 16, 2048, 7168, 8, 1, 4},
-    {FG_FP8_TENSOR, 1, 16384, 7168, 1, 1, 8},  {FG_FP8_TENSOR, 16, 16384, 7168, 1, 1, 8},
-    {FG_FP8_BLOCK128, 1, 2048, 7168, 8, 1, 8}, {FG_FP8_BLOCK128, 16, 2048, 7168, 8, 1, 8},
-    {FG_FP8_BLOCK128, 1, 16384, 7168, 1, 2, 5}, {FG_FP8_BLOCK128, 16, 16384, 7168, 1, 2, 5},
+    {FG_FP8_TENSOR, 1, 2048, 7168, 8, 2, 3},     {FG_FP8_TENSOR, 16, 2048, 7168, 8, 2, 3},
+    {FG_FP8_TENSOR, 1, 16384, 7168, 2, 2, 3},    {FG_FP8_TENSOR, 16, 16384, 7168, 2, 2, 3},
+    {FG_FP8_BLOCK128, 1, 2048, 7168, 8, 1, 4},   {FG_FP8_BLOCK128, 16, 2048, 7168, 8, 1, 4},
+    {FG_FP8_BLOCK128, 1, 16384, 7168, 2, 1, 4},  {FG_FP8_BLOCK128, 16, 16384, 7168, 2, 1, 4},
+    {FG_MXFP8, 1, 2048, 7168, 8, 1, 4},          {FG_MXFP8, 16, 2048, 7168, 8, 1, 4},
+    {FG_MXFP8, 1, 16384, 7168, 2, 1, 4},         {FG_MXFP8, 16, 16384, 7168, 2, 1, 4},
+    {FG_MXFP4, 1, 2048, 7168, 4, 4, 2},          {FG_MXFP4, 16, 2048, 7168, 4, 4, 2},
+    {FG_MXFP4, 1, 16384, 7168, 2, 1, 4},         {FG_MXFP4, 16, 16384, 7168, 2, 1, 4},
 };
 
 int64_t decode_row_limit() { return 32; }
@@ -170,7 +176,7 @@ fg_status make_plan(int mode, int64_t M, int64_t N, int64_t K, int split_k, fg_p
              (long long)M, (long long)N, (long long)K);
     return FG_OK;
   }
-  int split = split_k, sps = 2, stages = 5;
+  int split = split_k, sps = 1, stages = 4;
   bool from_table = false;
   for (const TableRow& r : kTable) {
     if (r.mode == mode && r.N == N && r.K == K && M <= r.m_max && (r.m_max == 1 ? M == 1 : M > 1)) {
@@ -182,12 +188,13 @@ fg_status make_plan(int mode, int64_t M, int64_t N, int64_t K, int split_k, fg_p
     }
   }
   if (split == 0) {
-    // smallest split in {1,2,4,8} that puts at least ~0.8 of a wave of CTAs on
-    // the SMs, keeping >= 4 slabs per split
-    const int64_t want = (static_cast<int64_t>(sm_count()) * 4) / 5;
+    // Heuristic (measured trend on GB300): the small-footprint pipeline (one
+    // slab per stage, four stages, up to three CTAs per SM) with the
+    // smallest split in {1,2,4,8} that gives at least 1.5 CTAs per SM,
+    // keeping >= 4 slabs per split.
+    const int64_t want = (static_cast<int64_t>(sm_count()) * 3) / 2;
     split = 1;
     while (split < 8 && tiles_n * tiles_m * split < want && KB / (split * 2) >= 4) split *= 2;
-    if (KB / split < 8) sps = 1, stages = 8;
   }
   // Sweep hook: FG_DECODE_CONFIG="<slabs per stage>,<stages>" overrides the
   // pipeline shape of every decode launch (refused when not instantiated).

@@ -82,7 +82,9 @@ def test_plan_heuristic_and_table(fg):
     p = fg.gemm_plan("fp8_tensor", 1, 2048, 7168)
     assert p["path"] == 0 and p["split_k"] == 8 and p["from_table"]
     p = fg.gemm_plan("fp8_tensor", 16, 16384, 7168)
-    assert p["split_k"] == 1 and p["ctas"] == 128
+    assert p["split_k"] == 2 and p["ctas"] == 256 and p["from_table"]
+    p = fg.gemm_plan("fp8_tensor", 8, 4096, 4096)          # heuristic: >= 1.5 CTAs per SM
+    assert not p["from_table"] and p["ctas"] >= 1.5 * 148
     p = fg.gemm_plan("fp8_tensor", 1, 2048, 7168, split_k=4)
     assert p["split_k"] == 4
     assert "sm103a" in p["name"] and "n2048" in p["name"] and "k7168" in p["name"]
