@@ -189,6 +189,23 @@ class OracleSample:
             "/".join(str(self.rows(c)) for c in self.wl["cases"]), len(self.wl["cases"]))
 
 
+# ---------------------------------------------------------- multi-rank
+
+def aggregate_ranks(ms, world, dist=None, device=None):
+    """Timed-region milliseconds of the slowest rank (every rank calls it)."""
+    if world <= 1:
+        return ms
+    import torch
+    t = torch.tensor([float(ms)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_value(steps, step_work, ms, world, unit_scale):
+    """Work of all ranks over the slowest rank's time (replicas: weak scaling)."""
+    return world * steps * step_work / (ms / 1e3) / unit_scale
+
+
 # ----------------------------------------------------------- ncu traffic
 
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "traffic.json")
@@ -388,14 +405,11 @@ def main():
     clocks = clk.stop()
     ms = t0.elapsed_time(t1)
     del graph
-    if world > 1:
-        tt = torch.tensor([ms], device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        ms = float(tt.item())
+    ms = aggregate_ranks(ms, world, dist, dev)
     if fg.get_error() != fg.FG_OK:
         raise RuntimeError("kernel error word set during the timed region")
     step_work = sum(x["work"] for x in cases)
-    value = world * K * step_work / (ms / 1e3) / scale_u
+    value = whole_job_value(K, step_work, ms, world, scale_u)
 
     # ---------------- per case: the main kernel alone, back to back (a graph
     # of the same call repeated, CUDA events around its replay)
@@ -439,8 +453,8 @@ def main():
             x["hY"].copy_(x["Y"], non_blocking=True)
     e1.record(stream)
     torch.cuda.synchronize()
-    e2e_ms = e0.elapsed_time(e1)
-    e2e_value = world * E * step_work / (e2e_ms / 1e3) / scale_u
+    e2e_ms = aggregate_ranks(e0.elapsed_time(e1), world, dist, dev)
+    e2e_value = whole_job_value(E, step_work, e2e_ms, world, scale_u)
 
     launches_per_step = sum((2 if x["S"] > 8 else 1) + (1 if x["plan"]["path"] == 1 and
                                                         x["c"]["mode"] in ("mxfp8", "mxfp4") else 0)
