@@ -257,6 +257,8 @@ fg_status make_tmap(CUtensorMap* map, const void* base, int64_t rows, int64_t rb
 
 }  // namespace
 
+bool pdl_enabled() { return getenv("FG_NO_PDL") == nullptr; }
+
 void set_error_message(const char* fmt, ...) {
   va_list ap;
   va_start(ap, fmt);

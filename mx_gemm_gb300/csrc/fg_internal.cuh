@@ -77,4 +77,8 @@ cudaError_t launch_reduce(const float* ws, int split, int64_t M, int64_t N, cons
 
 int sm_count();
 
+// Programmatic dependent launch is on unless FG_NO_PDL is set (a sweep hook
+// for measuring what the overlap is worth).
+bool pdl_enabled();
+
 }  // namespace fg

@@ -141,7 +141,7 @@ cudaError_t launch_reduce_s(const float* ws, int64_t mn4, const float* a_s, cons
   attr.id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr.val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = &attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = pdl_enabled() ? 1 : 0;
   return cudaLaunchKernelEx(&cfg, reduce_kernel<S>, reinterpret_cast<const float4*>(ws), mn4, a_s, b_s,
                             reinterpret_cast<uint2*>(y));
 }
