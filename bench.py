@@ -47,6 +47,11 @@ WORKLOADS = {
                                       kind="decode", idx=4),
     "mxfp4_decode_n16384_k7168": dict(cases=[dict(mode="mxfp4", M=m, N=16384, K=7168) for m in (1, 16)],
                                       kind="decode", idx=4, case_offset=3),
+    "mxfp8_b32_decode_n16384_k7168": dict(cases=[dict(mode="mxfp8_b32", M=m, N=16384, K=7168) for m in (1, 16)],
+                                          kind="decode", idx=5),
+    "bf16_decode_sweep_k7168": dict(cases=decode_cases("bf16"), kind="decode", idx=6),
+    "large_mxfp8_b32_4096x16384x7168": dict(cases=[dict(mode="mxfp8_b32", M=4096, N=16384, K=7168)], kind="large",
+                                            idx=5, case_offset=2),
     "large_mxfp8_4096x16384x7168": dict(cases=[dict(mode="mxfp8", M=4096, N=16384, K=7168)], kind="large",
                                         idx=4, case_offset=2),
     "large_mxfp4_4096x16384x7168": dict(cases=[dict(mode="mxfp4", M=4096, N=16384, K=7168)], kind="large",
@@ -66,7 +71,7 @@ def scale_bytes(mode, M, N, K):
         return 4 * (M + N // 128) * (K // 128)
     if mode == "mxfp8":
         return (M + N) * (K // 128)
-    if mode == "mxfp4":
+    if mode in ("mxfp4", "mxfp8_b32"):
         return (M + N) * (K // 32)
     return 0
 
@@ -159,7 +164,7 @@ class OracleSample:
         import oracle
         self.oracle = oracle
         self.orc = {"bf16": oracle.BF16, "fp8_tensor": oracle.FP8_TENSOR, "fp8_block128": oracle.FP8_BLOCK128,
-                    "mxfp8": oracle.MXFP8, "mxfp4": oracle.MXFP4}
+                    "mxfp8": oracle.MXFP8, "mxfp4": oracle.MXFP4, "mxfp8_b32": oracle.MXFP8_B32}
         self.wl, self.host_ops = wl, host_ops
         self.threads = os.cpu_count() or 1
         self.frac = 1.0 / 1024
@@ -177,7 +182,7 @@ class OracleSample:
             bs = b_s
             if c["mode"] == "fp8_block128":
                 bs = b_s[: (n + 127) // 128]
-            elif c["mode"] in ("mxfp8", "mxfp4"):
+            elif c["mode"] in ("mxfp8", "mxfp4", "mxfp8_b32"):
                 bs = b_s[:n]
             self.oracle.gemm(self.orc[c["mode"]], A, B[:n], a_s, bs, M=c["M"], N=n, K=c["K"],
                              threads=self.threads)
@@ -273,7 +278,7 @@ def main():
     off = wl.get("case_offset", 0)
     host_ops_fn = lambda: [case_operands(wl["idx"], i + off, c) for i, c in enumerate(wl["cases"])]  # noqa: E731
     dtype = {"bf16": "bf16", "fp8_tensor": "e4m3", "fp8_block128": "e4m3", "mxfp8": "e4m3",
-             "mxfp4": "e2m1"}[wl["cases"][0]["mode"]]
+             "mxfp4": "e2m1", "mxfp8_b32": "e4m3"}[wl["cases"][0]["mode"]]
 
     if args.impl == "reference":
         if rank != 0:
@@ -457,7 +462,7 @@ def main():
     e2e_value = whole_job_value(E, step_work, e2e_ms, world, scale_u)
 
     launches_per_step = sum((2 if x["S"] > 8 else 1) + (1 if x["plan"]["path"] == 1 and
-                                                        x["c"]["mode"] in ("mxfp8", "mxfp4") else 0)
+                                                        x["c"]["mode"] in ("mxfp8", "mxfp4", "mxfp8_b32") else 0)
                             for x in cases)
 
     cpu = None

@@ -10,7 +10,8 @@
  *    reduce that downcasts once at the final store), the direct-output
  *    epilogue for split_k = 1, the three scale modes (FP8 per-tensor, FP8
  *    128-block blockscale, MX: mxfp8 with one E8M0 per 128 K, mxfp4 with
- *    one E8M0 per 32 K), the weight/scale preshuffle helpers and the
+ *    one E8M0 per 32 K; the OCP-standard 32-element mxfp8 block is offered
+ *    beside the pages' 128-element one), the weight/scale preshuffle helpers and the
  *    shape-keyed dispatch; Copilot review: K must be a multiple of the scale
  *    block, and already-preshuffled weights must not be shuffled again.
  *  - FlyDSL PR "Enable the gmem->LDS async copy for f16/bf16 preshuffle
@@ -75,7 +76,8 @@ typedef enum fg_mode {
   FG_FP8_TENSOR = 1,   /* e4m3 A and B; fp32 scalars a_s, b_s                       */
   FG_FP8_BLOCK128 = 2, /* e4m3; a_s fp32 [M][K/128]; b_s fp32 [N/128][K/128]        */
   FG_MXFP8 = 3,        /* e4m3; E8M0 a_sf [M][K/128], b_sf [N][K/128]               */
-  FG_MXFP4 = 4         /* packed e2m1; E8M0 a_sf [M][K/32], b_sf [N][K/32]          */
+  FG_MXFP4 = 4,        /* packed e2m1; E8M0 a_sf [M][K/32], b_sf [N][K/32]          */
+  FG_MXFP8_B32 = 5     /* e4m3; E8M0 a_sf [M][K/32], b_sf [N][K/32] (OCP MX block)  */
 } fg_mode;
 
 /* fg_gemm flags */
@@ -102,11 +104,11 @@ typedef enum fg_mode {
  * 128-row tile is one contiguous copy.
  *
  * Scale image (sf): FP8_TENSOR: the fp32 b_s (16 bytes reserved);
- * FP8_BLOCK128: b_s fp32 [N/128][K/128] unchanged; MXFP8 / MXFP4: for each
- * 128-row tile and slab, 1 (MXFP8) or 2 (MXFP4) atoms of 512 bytes, atom
- * byte 16*(r%32) + 4*(r/32) + j = the E8M0 of row r for the j-th 32-K block
- * the atom covers (an MXFP8 128-K scale repeated for its four 32-K blocks);
- * BF16: none.
+ * FP8_BLOCK128: b_s fp32 [N/128][K/128] unchanged; MXFP8 / MXFP8_B32 /
+ * MXFP4: for each 128-row tile and slab, 1 (8-bit) or 2 (MXFP4) atoms of 512
+ * bytes, atom byte 16*(r%32) + 4*(r/32) + j = the E8M0 of row r for the j-th
+ * 32-K block the atom covers (an MXFP8 128-K scale repeated for its four
+ * 32-K blocks); BF16: none.
  */
 typedef struct fg_bshuf {
   uint32_t magic;
@@ -155,7 +157,7 @@ FG_API fg_status fg_preshuffle_b_size(int mode, int64_t N, int64_t K, uint64_t* 
  * One-time relayout of the weight B[N][K] (and of its scales) into the
  * images described above; fills *desc_out.  b_scales: FP8_TENSOR: device
  * fp32 scalar; FP8_BLOCK128: device fp32 [N/128][K/128]; MX: device uint8
- * E8M0 [N][K/128] or [N][K/32]; BF16: must be NULL.  B and the images must
+ * E8M0 [N][K/128] (MXFP8) or [N][K/32] (MXFP4, MXFP8_B32); BF16: must be NULL.  B and the images must
  * not overlap.  Errors: INVALID_ARG, SHAPE, ALIGN (16 bytes for B and the
  * images, 4 for fp32 scales), WORKSPACE (an image buffer smaller than
  * fg_preshuffle_b_size says), UNSUPPORTED_ARCH, CUDA.
@@ -192,7 +194,8 @@ FG_API fg_status fg_gemm_workspace_size(int mode, int64_t M, int64_t N, int64_t 
  * Y = dequant(A) . dequant(B)^T for the preshuffled weight `b`.
  *  A        device [M][K] codes (layout per mode, see top).
  *  a_scales FP8_TENSOR: device fp32 scalar; FP8_BLOCK128: fp32 [M][K/128];
- *           MXFP8: uint8 E8M0 [M][K/128]; MXFP4: uint8 E8M0 [M][K/32];
+ *           MXFP8: uint8 E8M0 [M][K/128]; MXFP4, MXFP8_B32: uint8 E8M0
+ *           [M][K/32];
  *           BF16: ignored (pass NULL).
  *  mode     must equal b->mode (FG_ERR_LAYOUT otherwise).
  *  split_k  0 = dispatch chooses; 1..16 = number of K splits.  Split s takes

@@ -14,8 +14,8 @@ Recipe (the pages measure on bare GEMM shapes, not on a dataset):
     code = e4m3(x_block / scale);
   * MX: per 1 x blk block, E8M0 c = 127 + ceil(log2(amax / elem_max)), clamped
     to [0, 254] (an all-zero block gets 127); code = RNE(x / 2^(c-127)) in the
-    element format (e4m3, elem_max 448, blk 128; or e2m1, elem_max 6, blk 32,
-    two codes per byte, low nibble = even k).
+    element format (e4m3, elem_max 448, blk 128 -- or 32 for the OCP block;
+    or e2m1, elem_max 6, blk 32, two codes per byte, low nibble = even k).
 e4m3 and bf16 encodings use torch's dtype casts; e2m1 rounding is done here
 (ties to the even code) and pinned against an independent dtype library in
 the CPU tests.
@@ -24,7 +24,7 @@ import math
 
 import numpy as np
 
-MODES = ("bf16", "fp8_tensor", "fp8_block128", "mxfp8", "mxfp4")
+MODES = ("bf16", "fp8_tensor", "fp8_block128", "mxfp8", "mxfp4", "mxfp8_b32")
 E4M3_MAX = 448.0
 E2M1_MAX = 6.0
 _E2M1_MAG = np.array([0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0], np.float64)
@@ -126,15 +126,16 @@ def fp8_block128_operand(rows, K, seed, scale_seed, block_rows):
 
 def mx_operand(rows, K, seed, fmt):
     """MX operand: fmt 'mxfp8' -> (e4m3 codes [rows][K], E8M0 [rows][K/128]);
-    fmt 'mxfp4' -> (packed e2m1 [rows][K/2], E8M0 [rows][K/32])."""
-    blk, emax = (128, E4M3_MAX) if fmt == "mxfp8" else (32, E2M1_MAX)
+    'mxfp8_b32' -> (e4m3 codes [rows][K], E8M0 [rows][K/32]);
+    'mxfp4' -> (packed e2m1 [rows][K/2], E8M0 [rows][K/32])."""
+    blk, emax = {"mxfp8": (128, E4M3_MAX), "mxfp8_b32": (32, E4M3_MAX), "mxfp4": (32, E2M1_MAX)}[fmt]
     assert K % blk == 0
     x = randn(rows, K, seed).reshape(rows, K // blk, blk)
     amax = np.max(np.abs(x), axis=2)
     c = e8m0_for(amax, emax)
     scale = np.ldexp(1.0, c.astype(np.int64) - 127)
     q = (x.astype(np.float64) / scale[:, :, None]).reshape(rows, K)
-    if fmt == "mxfp8":
+    if fmt in ("mxfp8", "mxfp8_b32"):
         return to_e4m3_codes(q.astype(np.float32)), c
     return pack_e2m1(to_e2m1_codes(q)), c
 
@@ -151,7 +152,7 @@ def operands(mode, M, N, K, seed_a, seed_b, seed_s):
         A, a_s = fp8_block128_operand(M, K, seed_a, seed_s, 1)
         B, b_s = fp8_block128_operand(N, K, seed_b, seed_s + 500, 128)
         return A, B, a_s, b_s
-    if mode in ("mxfp8", "mxfp4"):
+    if mode in ("mxfp8", "mxfp4", "mxfp8_b32"):
         A, a_s = mx_operand(M, K, seed_a, mode)
         B, b_s = mx_operand(N, K, seed_b, mode)
         return A, B, a_s, b_s

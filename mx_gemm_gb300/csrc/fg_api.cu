@@ -46,10 +46,10 @@ fg_status cuda_fail(cudaError_t e, const char* what) {
 
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
 
-bool mode_ok(int mode) { return mode >= FG_BF16 && mode <= FG_MXFP4; }
+bool mode_ok(int mode) { return mode >= FG_BF16 && mode <= FG_MXFP8_B32; }
 
 const char* mode_name(int mode) {
-  static const char* names[] = {"bf16", "fp8_tensor", "fp8_block128", "mxfp8", "mxfp4"};
+  static const char* names[] = {"bf16", "fp8_tensor", "fp8_block128", "mxfp8", "mxfp4", "mxfp8_b32"};
   return mode_ok(mode) ? names[mode] : "?";
 }
 
@@ -118,7 +118,8 @@ uint64_t sf_image_bytes(int mode, int64_t N, int64_t K) {
   switch (mode) {
     case FG_FP8_TENSOR: return 16;
     case FG_FP8_BLOCK128: return static_cast<uint64_t>(N / 128) * (K / 128) * 4;
-    case FG_MXFP8: return static_cast<uint64_t>(N / 128) * (K / 128) * 512;
+    case FG_MXFP8:
+    case FG_MXFP8_B32: return static_cast<uint64_t>(N / 128) * (K / 128) * 512;
     case FG_MXFP4: return static_cast<uint64_t>(N / 128) * (K / 256) * 2 * 512;
     default: return 0;
   }
@@ -331,7 +332,7 @@ fg_status fg_preshuffle_b(int mode, const void* B, const void* b_scales, int64_t
   if (mode != FG_BF16 && (!b_scales || !sf_image)) return fail(FG_ERR_INVALID_ARG, "%s needs B scales and a scale image", mode_name(mode));
   if (!aligned(B, 16) || !aligned(b_image, 16) || (sf_image && !aligned(sf_image, 16)))
     return fail(FG_ERR_ALIGN, "B and the images must be 16-byte aligned");
-  if (b_scales && !aligned(b_scales, (mode == FG_MXFP8 || mode == FG_MXFP4) ? 1 : 4))
+  if (b_scales && !aligned(b_scales, is_mx(mode) ? 1 : 4))
     return fail(FG_ERR_ALIGN, "fp32 scales must be 4-byte aligned");
   if (b_image_bytes < need_b || sf_image_bytes < need_sf)
     return fail(FG_ERR_WORKSPACE, "image buffers too small (need %llu and %llu bytes)", (unsigned long long)need_b,
@@ -346,7 +347,7 @@ fg_status fg_preshuffle_b(int mode, const void* B, const void* b_scales, int64_t
   if (mode == FG_FP8_TENSOR || mode == FG_FP8_BLOCK128) {
     e = cudaMemcpyAsync(sf_image, b_scales, mode == FG_FP8_TENSOR ? 4 : need_sf, cudaMemcpyDeviceToDevice, st);
     if (e != cudaSuccess) return cuda_fail(e, "scale copy");
-  } else if (mode == FG_MXFP8 || mode == FG_MXFP4) {
+  } else if (is_mx(mode)) {
     e = launch_relayout_sf(mode, static_cast<const uint8_t*>(b_scales), static_cast<uint8_t*>(sf_image), N, K, false,
                            st);
     if (e != cudaSuccess) return cuda_fail(e, "scale relayout launch");
@@ -407,7 +408,7 @@ fg_status fg_gemm_workspace_size(int mode, int64_t M, int64_t N, int64_t K, int 
   fg_status s = fg_gemm_plan(mode, M, N, K, split_k, &plan);
   if (s != FG_OK) return s;
   if (plan.path == 1)
-    *bytes = (mode == FG_MXFP8 || mode == FG_MXFP4) ? sf_rows_image_bytes(mode, M, K) : 0;
+    *bytes = is_mx(mode) ? sf_rows_image_bytes(mode, M, K) : 0;
   else
     *bytes = plan.split_k > kMaxClusterSplit ? static_cast<uint64_t>(plan.split_k) * M * N * 4 : 0;
   return FG_OK;
@@ -436,7 +437,7 @@ fg_status fg_gemm(const void* A, const void* a_scales, int64_t M, const fg_bshuf
   if ((s = make_plan(mode, M, N, K, split_k, &plan)) != FG_OK) return s;
   const int split = plan.split_k;
   const bool defer = (flags & FG_FLAG_DEFER_REDUCE) != 0;
-  const bool mx = mode == FG_MXFP8 || mode == FG_MXFP4;
+  const bool mx = is_mx(mode);
   const bool fused = plan.path == 0 && split > 1 && split <= kMaxClusterSplit && !defer;
   if (split > 1 && !fused) {
     const uint64_t need = static_cast<uint64_t>(split) * M * N * 4;

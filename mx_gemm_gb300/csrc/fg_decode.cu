@@ -69,7 +69,7 @@ constexpr int kTokRows = 16;
 
 template <int MODE, int SPS, int STAGES>
 struct DCfg {
-  static constexpr int APS = MODE == kMXFP4 ? 2 : (MODE == kMXFP8 ? 1 : 0);
+  static constexpr int APS = MODE == kMXFP4 ? 2 : ((MODE == kMXFP8 || MODE == kMXFP8B32) ? 1 : 0);
   static constexpr int B_BYTES = SPS * kSlabBytes;
   static constexpr int A_BYTES = SPS * kTokSlabBytes;
   static constexpr int SFW_BYTES = SPS * APS * 512;
@@ -243,7 +243,7 @@ __global__ void __launch_bounds__(kThreads, 1)
               mma_f16(d, adesc, bdesc, idesc_bf16(128, kTokRows), acc);
             } else if (MODE == kTensor || MODE == kBlock) {
               mma_f8f6f4(d, adesc, bdesc, idesc_e4m3(128, kTokRows), acc);
-            } else if (MODE == kMXFP8) {
+            } else if (MODE == kMXFP8 || MODE == kMXFP8B32) {
               mma_mxf8f6f4(d, adesc, bdesc, mx_idesc(MODE, j), tmem + sfw_col + 4 * v, tmem + sft_col + 4 * v, acc);
             } else {
               const int t = v * 2 + (j >> 1);
@@ -299,7 +299,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           uint32_t wv = 0x7F7F7F7Fu;  // 2^0 for padded rows (their values are zero)
           if (row < p.M) {
             const int q32 = ((u0 + ub) * C::APS + t) * 4;  // first 32-K block of the atom
-            if (MODE == kMXFP4) {
+            if (MODE != kMXFP8) {   // one scale per 32-K block
               const uint8_t* src = asf + static_cast<size_t>(row) * (p.K / 32) + q32;
               wv = static_cast<uint32_t>(src[0]) | (static_cast<uint32_t>(src[1]) << 8) |
                    (static_cast<uint32_t>(src[2]) << 16) | (static_cast<uint32_t>(src[3]) << 24);
@@ -493,7 +493,7 @@ cudaError_t launch_one(const CUtensorMap& tmap_a, const DecodeParams& p, dim3 gr
 }  // namespace
 
 bool decode_config_supported(const DecodeConfig& c) {
-  if (c.mode < kBF16 || c.mode > kMXFP4) return false;
+  if (c.mode < kBF16 || c.mode > kMXFP8B32) return false;
   return (c.sps == 1 && (c.stages == 4 || c.stages == 8)) || (c.sps == 2 && (c.stages == 3 || c.stages == 5)) ||
          (c.sps == 4 && c.stages == 2);
 }
@@ -507,6 +507,7 @@ cudaError_t launch_decode(const DecodeConfig& c, const CUtensorMap& tmap_a, cons
   FG_DECODE_CONFIGS(FG_TRY, kBlock)
   FG_DECODE_CONFIGS(FG_TRY, kMXFP8)
   FG_DECODE_CONFIGS(FG_TRY, kMXFP4)
+  FG_DECODE_CONFIGS(FG_TRY, kMXFP8B32)
 #undef FG_TRY
   return cudaErrorInvalidValue;
 }

@@ -8,12 +8,16 @@
 
 namespace fg {
 
-enum Mode : int { kBF16 = 0, kTensor = 1, kBlock = 2, kMXFP8 = 3, kMXFP4 = 4 };
+enum Mode : int { kBF16 = 0, kTensor = 1, kBlock = 2, kMXFP8 = 3, kMXFP4 = 4, kMXFP8B32 = 5 };
+
+inline bool is_mx(int mode) { return mode == kMXFP8 || mode == kMXFP4 || mode == kMXFP8B32; }
+// MX scale columns per row: one per 128 K (mxfp8) or per 32 K.
+inline int64_t mx_sf_cols(int mode, int64_t K) { return mode == kMXFP8 ? K / 128 : K / 32; }
 
 inline int elem_bits(int mode) { return mode == kBF16 ? 16 : (mode == kMXFP4 ? 4 : 8); }
 inline int64_t row_bytes(int mode, int64_t K) { return K * elem_bits(mode) / 8; }
 // 512-byte scale-factor atoms per 128-byte K slab of the weight image.
-inline int sf_atoms_per_slab(int mode) { return mode == kMXFP4 ? 2 : (mode == kMXFP8 ? 1 : 0); }
+inline int sf_atoms_per_slab(int mode) { return mode == kMXFP4 ? 2 : (is_mx(mode) ? 1 : 0); }
 
 // Parameters of the split-K decode kernel (weights on the MMA M side,
 // tokens on the N side, 16 tokens per CTA tile).

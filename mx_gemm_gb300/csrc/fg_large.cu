@@ -377,7 +377,7 @@ __global__ void __launch_bounds__(kMxThreads, 1)
           for (int j = 0; j < 4; ++j) {
             const uint64_t adesc = sdesc_sw128(smem_u32(st + j * 32));
             const uint64_t bdesc = sdesc_sw128(smem_u32(st + kABytes + j * 32));
-            if (MODE == kMXFP8) {
+            if (MODE == kMXFP8 || MODE == kMXFP8B32) {
               mma_mxf8f6f4(tmem, adesc, bdesc, idesc_mx(kBM, kBN, 0u, j, j), tmem + sfa, tmem + sfb, (kb | j) != 0);
             } else {
               const int g = j >> 1, id = 2 * (j & 1);
@@ -466,12 +466,13 @@ cudaError_t launch_mx(const CUtensorMap& tmap_a, const LargeParams& p, int ctas,
 
 }  // namespace
 
-bool large_supported(int mode) { return mode == kBF16 || mode == kTensor || mode == kMXFP8 || mode == kMXFP4; }
+bool large_supported(int mode) { return mode == kBF16 || mode == kTensor || is_mx(mode); }
 
 cudaError_t launch_large(int mode, const CUtensorMap& tmap_a, const LargeParams& p, int ctas, cudaStream_t stream) {
   if (mode == kBF16) return launch_mode<kBF16>(tmap_a, p, ctas, stream);
   if (mode == kTensor) return launch_mode<kTensor>(tmap_a, p, ctas, stream);
   if (mode == kMXFP8) return launch_mx<kMXFP8>(tmap_a, p, ctas, stream);
+  if (mode == kMXFP8B32) return launch_mx<kMXFP8B32>(tmap_a, p, ctas, stream);
   if (mode == kMXFP4) return launch_mx<kMXFP4>(tmap_a, p, ctas, stream);
   return cudaErrorNotSupported;
 }

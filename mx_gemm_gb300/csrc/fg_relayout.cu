@@ -48,12 +48,13 @@ __global__ void relayout_b_kernel(const uint4* __restrict__ src, uint4* __restri
 // MX weight scales [N][K/blk] (E8M0 bytes) <-> atoms of 512 bytes: for each
 // 128-row tile nb, slab u and atom a of the slab, byte 16*(r%32) + 4*(r/32) + j
 // holds the scale of row nb*128 + r for the 32-K block (u*APS + a)*4 + j.
-// mxfp8 scales cover 128 K, so the four 32-K blocks of a slab repeat one.
+// mxfp8 scales cover 128 K, so the four 32-K blocks of a slab repeat one;
+// mxfp4 and the 32-block mxfp8 have one scale per 32-K block.
 __global__ void relayout_sf_kernel(const uint8_t* __restrict__ src, uint8_t* __restrict__ dst, int64_t N, int64_t K,
                                    int mode, int inverse) {
   const int aps = mode == kMXFP4 ? 2 : 1;
   const int64_t KB = mode == kMXFP4 ? K / 256 : K / 128;  // slabs per row
-  const int64_t sf_cols = mode == kMXFP4 ? K / 32 : K / 128;
+  const int64_t sf_cols = mode == kMXFP8 ? K / 128 : K / 32;
   const int64_t total = (N / 128) * KB * aps * 512;
   for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < total;
        i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
@@ -65,10 +66,10 @@ __global__ void relayout_sf_kernel(const uint8_t* __restrict__ src, uint8_t* __r
     const int64_t rem = atom - nb * KB * aps;
     const int64_t q32 = rem * 4 + j;  // (u*aps + a)*4 + j
     const int64_t n = nb * 128 + r;
-    const int64_t col = mode == kMXFP4 ? q32 : (q32 >> 2);
+    const int64_t col = mode == kMXFP8 ? (q32 >> 2) : q32;
     if (!inverse) {
       dst[i] = __ldg(src + n * sf_cols + col);
-    } else if (mode == kMXFP4 || j == 0) {
+    } else if (mode != kMXFP8 || j == 0) {
       dst[n * sf_cols + col] = __ldg(src + i);
     }
   }
@@ -81,7 +82,7 @@ __global__ void relayout_sf_rows_kernel(const uint8_t* __restrict__ src, uint8_t
                                         int64_t K, int mode) {
   const int aps = mode == kMXFP4 ? 2 : 1;
   const int64_t KB = mode == kMXFP4 ? K / 256 : K / 128;
-  const int64_t sf_cols = mode == kMXFP4 ? K / 32 : K / 128;
+  const int64_t sf_cols = mode == kMXFP8 ? K / 128 : K / 32;
   const int64_t total = ((rows + 127) / 128) * KB * aps * 512;
   for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < total;
        i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
@@ -92,7 +93,7 @@ __global__ void relayout_sf_rows_kernel(const uint8_t* __restrict__ src, uint8_t
     const int64_t mb = atom / (KB * aps);
     const int64_t q32 = (atom - mb * KB * aps) * 4 + j;
     const int64_t m = mb * 128 + r;
-    const int64_t col = mode == kMXFP4 ? q32 : (q32 >> 2);
+    const int64_t col = mode == kMXFP8 ? (q32 >> 2) : q32;
     dst[i] = m < rows ? __ldg(src + m * sf_cols + col) : uint8_t(127);
   }
 }

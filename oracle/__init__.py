@@ -19,9 +19,9 @@ import numpy as np
 
 from . import build as _build
 
-BF16, FP8_TENSOR, FP8_BLOCK128, MXFP8, MXFP4 = 0, 1, 2, 3, 4
+BF16, FP8_TENSOR, FP8_BLOCK128, MXFP8, MXFP4, MXFP8_B32 = 0, 1, 2, 3, 4, 5
 MODE_NAMES = {BF16: "bf16", FP8_TENSOR: "fp8_tensor", FP8_BLOCK128: "fp8_block128",
-              MXFP8: "mxfp8", MXFP4: "mxfp4"}
+              MXFP8: "mxfp8", MXFP4: "mxfp4", MXFP8_B32: "mxfp8_b32"}
 
 _lib = None
 
@@ -101,7 +101,8 @@ def gemm(mode, A, B, a_scale=None, b_scale=None, M=None, N=None, K=None,
     A, B are the raw codes as numpy arrays: uint16 bf16 bits [M][K],
     uint8 e4m3 codes [M][K], or uint8 packed e2m1 pairs [M][K/2].  Scales:
     fp32 scalars (FP8_TENSOR), fp32 [M][K/128] and [N/128][K/128]
-    (FP8_BLOCK128), uint8 E8M0 [M][K/128] (MXFP8) or [M][K/32] (MXFP4).
+    (FP8_BLOCK128), uint8 E8M0 [M][K/128] (MXFP8) or [M][K/32] (MXFP4,
+    MXFP8_B32).
     ``tensor_scale`` False gives the unscaled per-tensor sum, which is what a
     split-K partial holds in that mode.
     """
@@ -118,7 +119,7 @@ def gemm(mode, A, B, a_scale=None, b_scale=None, M=None, N=None, K=None,
     if mode in (FP8_TENSOR, FP8_BLOCK128):
         a_scale = _c(np.asarray(a_scale, np.float32).reshape(-1), np.float32)
         b_scale = _c(np.asarray(b_scale, np.float32).reshape(-1), np.float32)
-    elif mode in (MXFP8, MXFP4):
+    elif mode in (MXFP8, MXFP4, MXFP8_B32):
         a_scale, b_scale = _c(a_scale, np.uint8), _c(b_scale, np.uint8)
     else:
         a_scale = b_scale = None

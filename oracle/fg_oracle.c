@@ -23,6 +23,8 @@
  *   MXFP8        Ad = e4m3(a) * 2^(a_sf[m][k/128]-127)     ("mx128")
  *   MXFP4        Ad = e2m1(a) * 2^(a_sf[m][k/32]-127), two e2m1 codes per
  *                byte, low nibble = even k
+ *   MXFP8_B32    Ad = e4m3(a) * 2^(a_sf[m][k/32]-127)      (the OCP MX block of
+ *                32 elements, next to the pages' 128-element "mx128")
  * and the same for B with n in place of m.
  *
  * Encodings are decoded from their bit fields through 256-entry tables built
@@ -44,7 +46,8 @@ enum {
     ORC_FP8_TENSOR = 1,
     ORC_FP8_BLOCK128 = 2,
     ORC_MXFP8 = 3,
-    ORC_MXFP4 = 4
+    ORC_MXFP4 = 4,
+    ORC_MXFP8_B32 = 5
 };
 
 /* ---------------------------------------------------------------- decoding */
@@ -163,6 +166,11 @@ static double dequant(const orc_job *j, int is_b, int64_t r, int64_t k)
         const double s = T_E8M0[((const uint8_t *)S)[r * kb + k / 128]];
         return T_E4M3[((const uint8_t *)X)[r * K + k]] * s;
     }
+    case ORC_MXFP8_B32: {
+        const int64_t kb = ceil_div(K, 32);
+        const double s = T_E8M0[((const uint8_t *)S)[r * kb + k / 32]];
+        return T_E4M3[((const uint8_t *)X)[r * K + k]] * s;
+    }
     case ORC_MXFP4: {
         const int64_t kb = ceil_div(K, 32);
         const double s = T_E8M0[((const uint8_t *)S)[r * kb + k / 32]];
@@ -210,7 +218,7 @@ int orc_gemm(int mode, int64_t M, int64_t N, int64_t K,
              int tensor_scale, double *out, int threads)
 {
     ensure_tables();
-    if (mode < ORC_BF16 || mode > ORC_MXFP4 || M < 0 || N < 0 || K < 0)
+    if (mode < ORC_BF16 || mode > ORC_MXFP8_B32 || M < 0 || N < 0 || K < 0)
         return -1;
     if (k0 < 0 || k1 > K || k0 > k1)
         return -1;
@@ -261,7 +269,7 @@ int orc_splitk_range(int mode, int64_t K, int S, int s, int64_t *k_begin, int64_
         per_unit = 64;
     else if (mode == ORC_MXFP4)
         per_unit = 256;
-    else if (mode >= ORC_FP8_TENSOR && mode <= ORC_MXFP8)
+    else if ((mode >= ORC_FP8_TENSOR && mode <= ORC_MXFP8) || mode == ORC_MXFP8_B32)
         per_unit = 128;
     else
         return -1;
@@ -343,24 +351,24 @@ void orc_round_bf16(const double *in, int64_t n, uint16_t *out)
  * two for mxfp4), a 512-byte atom whose byte 16*(r%32) + 4*(r/32) + j holds
  * the E8M0 scale of row nb*128 + r for the 32-K block (u*atoms + a)*4 + j.
  * An mxfp8 scale covers 128 K, i.e. the four 32-K blocks of its slab.
- * sf is [N][K/128] (mxfp8) or [N][K/32] (mxfp4).
+ * sf is [N][K/128] (mxfp8) or [N][K/32] (mxfp4, mxfp8 with 32-K blocks).
  */
 int orc_sf_image(int mode, const uint8_t *sf, int64_t N, int64_t K, uint8_t *out)
 {
-    if ((mode != ORC_MXFP8 && mode != ORC_MXFP4) || N % 128 != 0)
+    if ((mode != ORC_MXFP8 && mode != ORC_MXFP4 && mode != ORC_MXFP8_B32) || N % 128 != 0)
         return -1;
     const int64_t slab_k = mode == ORC_MXFP4 ? 256 : 128;
     if (K % slab_k != 0)
         return -1;
     const int64_t atoms = mode == ORC_MXFP4 ? 2 : 1;
     const int64_t slabs = K / slab_k;
-    const int64_t cols = mode == ORC_MXFP4 ? K / 32 : K / 128;
+    const int64_t cols = mode == ORC_MXFP8 ? K / 128 : K / 32;
     for (int64_t n = 0; n < N; ++n)
         for (int64_t q = 0; q < K / 32; ++q) {          /* 32-K block index */
             const int64_t nb = n / 128, r = n % 128;
             const int64_t u = q / (4 * atoms), a = (q / 4) % atoms, j = q % 4;
             const int64_t atom = (nb * slabs + u) * atoms + a;
-            const uint8_t v = mode == ORC_MXFP4 ? sf[n * cols + q] : sf[n * cols + q / 4];
+            const uint8_t v = mode == ORC_MXFP8 ? sf[n * cols + q / 4] : sf[n * cols + q];
             out[atom * 512 + 16 * (r % 32) + 4 * (r / 32) + j] = v;
         }
     return 0;

@@ -8,7 +8,7 @@ import oracle
 from tests import parity
 
 ORC = {"bf16": oracle.BF16, "fp8_tensor": oracle.FP8_TENSOR, "fp8_block128": oracle.FP8_BLOCK128,
-       "mxfp8": oracle.MXFP8, "mxfp4": oracle.MXFP4}
+       "mxfp8": oracle.MXFP8, "mxfp4": oracle.MXFP4, "mxfp8_b32": oracle.MXFP8_B32}
 
 
 def dev(x):

@@ -15,7 +15,7 @@ from tests.gpu_util import Case, dev, host, y_to_f64
 
 pytestmark = pytest.mark.gpu
 
-MODES = ["bf16", "fp8_tensor", "fp8_block128", "mxfp8", "mxfp4"]
+MODES = ["bf16", "fp8_tensor", "fp8_block128", "mxfp8", "mxfp4", "mxfp8_b32"]
 
 
 def _slabs(mode, K):
@@ -64,14 +64,16 @@ def test_deferred_reduce_equals_fused_call(mode, S):
     assert torch.equal(y_two.view(torch.int16), y_one.view(torch.int16))
 
 
-ONE = {"bf16": 0x3F80, "fp8_tensor": 0x38, "fp8_block128": 0x38, "mxfp8": 0x38, "mxfp4": 0x2}
+ONE = {"bf16": 0x3F80, "fp8_tensor": 0x38, "fp8_block128": 0x38, "mxfp8": 0x38, "mxfp4": 0x2,
+       "mxfp8_b32": 0x38}
 
 
 def _unit_a_scales(mode, M, K):
     return {"fp8_tensor": np.array([1.0], np.float32),
             "fp8_block128": np.ones((M, K // 128), np.float32),
             "mxfp8": np.full((M, K // 128), 127, np.uint8),
-            "mxfp4": np.full((M, K // 32), 127, np.uint8)}.get(mode)
+            "mxfp4": np.full((M, K // 32), 127, np.uint8),
+            "mxfp8_b32": np.full((M, K // 32), 127, np.uint8)}.get(mode)
 
 
 @pytest.mark.parametrize("mode", MODES)
@@ -104,7 +106,8 @@ def test_all_ones_is_exact(mode):
                 ONE[mode] if mode != "mxfp4" else 0x22, np.uint16 if mode == "bf16" else np.uint8)
     B = np.full((N, A.shape[1]), A.flat[0], A.dtype)
     b_s = {"fp8_tensor": np.array([1.0], np.float32), "fp8_block128": np.ones((1, K // 128), np.float32),
-           "mxfp8": np.full((N, K // 128), 127, np.uint8), "mxfp4": np.full((N, K // 32), 127, np.uint8)}.get(mode)
+           "mxfp8": np.full((N, K // 128), 127, np.uint8), "mxfp4": np.full((N, K // 32), 127, np.uint8),
+           "mxfp8_b32": np.full((N, K // 32), 127, np.uint8)}.get(mode)
     c = Case(mode, A, B, _unit_a_scales(mode, M, K), b_s)
     for S in (1, 4):
         y = y_to_f64(c.gemm(split_k=S))
@@ -116,7 +119,7 @@ def test_all_ones_is_exact(mode):
 DECODE = [(m, n) for m, n in inputs.DECODE_SHAPES]
 
 
-@pytest.mark.parametrize("mode", ["fp8_tensor", "fp8_block128", "mxfp8", "mxfp4"])
+@pytest.mark.parametrize("mode", ["fp8_tensor", "fp8_block128", "mxfp8", "mxfp4", "mxfp8_b32"])
 @pytest.mark.parametrize("M,N", DECODE)
 def test_decode_workload_parity(mode, M, N):
     """The pages' decode shapes (K=7168) in the dispatch-chosen configuration,

@@ -17,7 +17,7 @@ def _kb(mode, K):
     return K * 2 if mode == "bf16" else (K // 2 if mode == "mxfp4" else K)
 
 
-@pytest.mark.parametrize("mode", ["bf16", "fp8_tensor", "fp8_block128", "mxfp8", "mxfp4"])
+@pytest.mark.parametrize("mode", ["bf16", "fp8_tensor", "fp8_block128", "mxfp8", "mxfp4", "mxfp8_b32"])
 @pytest.mark.parametrize("N,K", [(128, 256), (384, 1536), (256, 7168)])
 def test_relayout_matches_spec_and_inverts(mode, N, K):
     A, B, a_s, b_s = inputs.operands(mode, 1, N, K, 5, 6, 7)
@@ -26,9 +26,9 @@ def test_relayout_matches_spec_and_inverts(mode, N, K):
     kb = _kb(mode, K)
     spec = oracle.preshuffle_b(np.ascontiguousarray(B).view(np.uint8).reshape(N, kb), N, kb)
     assert np.array_equal(host(pb.data), spec)
-    if mode in ("mxfp8", "mxfp4"):
-        assert np.array_equal(host(pb.sf), oracle.sf_image(oracle.MXFP8 if mode == "mxfp8" else oracle.MXFP4,
-                                                          b_s, N, K))
+    if mode in ("mxfp8", "mxfp4", "mxfp8_b32"):
+        orc_mode = {"mxfp8": oracle.MXFP8, "mxfp4": oracle.MXFP4, "mxfp8_b32": oracle.MXFP8_B32}[mode]
+        assert np.array_equal(host(pb.sf), oracle.sf_image(orc_mode, b_s, N, K))
     back, sc = fg.unshuffle_b(pb)
     torch.cuda.synchronize()
     assert np.array_equal(host(back), np.ascontiguousarray(B).view(np.uint8).reshape(N, kb))

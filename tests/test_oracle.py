@@ -24,7 +24,7 @@ from tests import parity
 
 ml = pytest.importorskip("ml_dtypes")
 
-MODES = [oracle.BF16, oracle.FP8_TENSOR, oracle.FP8_BLOCK128, oracle.MXFP8, oracle.MXFP4]
+MODES = [oracle.BF16, oracle.FP8_TENSOR, oracle.FP8_BLOCK128, oracle.MXFP8, oracle.MXFP4, oracle.MXFP8_B32]
 
 
 # ------------------------------------------------------------ decode tables
@@ -93,7 +93,7 @@ def _frac_values(mode, X, S, rows, K, is_b):
             for k in range(K):
                 sr = r // 128 if is_b else r
                 out[r][k] *= Fraction(float(np.float32(S.reshape(-1)[sr * kb + k // 128])))
-    elif mode in (oracle.MXFP8, oracle.MXFP4):
+    elif mode in (oracle.MXFP8, oracle.MXFP4, oracle.MXFP8_B32):
         blk = 128 if mode == oracle.MXFP8 else 32
         kb = -(-K // blk)
         sv = S.reshape(-1).view(ml.float8_e8m0fnu).astype(np.float64)
@@ -178,7 +178,7 @@ def test_bruteforce_catches_transposed_operand():
 # ----------------------------------------------------------- closed forms
 
 ONE = {oracle.BF16: 0x3F80, oracle.FP8_TENSOR: 0x38, oracle.FP8_BLOCK128: 0x38,
-       oracle.MXFP8: 0x38, oracle.MXFP4: 0x2}
+       oracle.MXFP8: 0x38, oracle.MXFP4: 0x2, oracle.MXFP8_B32: 0x38}
 
 
 def _unit_scales(mode, rows, K):
@@ -188,7 +188,7 @@ def _unit_scales(mode, rows, K):
         return np.ones((rows, K // 128), np.float32)
     if mode == oracle.MXFP8:
         return np.full((rows, K // 128), 127, np.uint8)
-    if mode == oracle.MXFP4:
+    if mode in (oracle.MXFP4, oracle.MXFP8_B32):
         return np.full((rows, K // 32), 127, np.uint8)
     return None
 
@@ -279,9 +279,9 @@ def test_mxfp4_nibble_order_low_is_even_k():
 
 # ----------------------------------------------------- split invariance
 
-@pytest.mark.parametrize("mode", [oracle.FP8_TENSOR, oracle.MXFP8, oracle.MXFP4])
+@pytest.mark.parametrize("mode", [oracle.FP8_TENSOR, oracle.MXFP8, oracle.MXFP4, oracle.MXFP8_B32])
 def test_split_sums_are_exact(mode):
-    name = {oracle.FP8_TENSOR: "fp8_tensor", oracle.MXFP8: "mxfp8", oracle.MXFP4: "mxfp4"}[mode]
+    name = oracle.MODE_NAMES[mode]
     M, N, K = 5, 128, 2048
     A, B, a_s, b_s = inputs.operands(name, M, N, K, 11, 12, 13)
     y = oracle.gemm(mode, A, B, a_s, b_s, tensor_scale=False, threads=4)
@@ -313,7 +313,7 @@ def test_splitk_partition():
              for s in range(8)]
     assert sizes == [4, 4, 4, 4, 3, 3, 3, 3]
     for mode, K in [(oracle.BF16, 8192), (oracle.FP8_BLOCK128, 7168), (oracle.MXFP4, 7168),
-                    (oracle.MXFP8, 128)]:
+                    (oracle.MXFP8, 128), (oracle.MXFP8_B32, 7168)]:
         for S in (1, 2, 3, 4, 8):
             rs = [oracle.splitk_range(mode, K, S, s) for s in range(S)]
             assert rs[0][0] == 0 and rs[-1][1] == K
@@ -374,7 +374,7 @@ def test_e2m1_rounding_matches_ml_dtypes():
 
 
 def test_e8m0_choice_bounds_block():
-    for fmt, emax in (("mxfp8", 448.0), ("mxfp4", 6.0)):
+    for fmt, emax in (("mxfp8", 448.0), ("mxfp4", 6.0), ("mxfp8_b32", 448.0)):
         A, sf = inputs.mx_operand(64, 1024, 5, fmt)
         blk = 128 if fmt == "mxfp8" else 32
         x = inputs.randn(64, 1024, 5).reshape(64, -1, blk)
@@ -405,3 +405,22 @@ def test_tolerance_check_catches_planted_mistakes():
     assert parity.ws_violations(dropped, ref)[0] > 0
     bs_swapped = oracle.gemm(oracle.FP8_BLOCK128, A, B, a_s, b_s[::-1].copy())
     assert parity.y_violations(bs_swapped, ref)[0] > 0
+
+
+def test_sf_image_spec_is_a_bijection_onto_atoms():
+    """Every (row, 32-K block) scale lands in exactly one atom byte; the
+    128-K mxfp8 scale fills the four 32-K bytes of its slab."""
+    for mode, cols_per_row, K in ((oracle.MXFP4, 7168 // 32, 7168), (oracle.MXFP8_B32, 1024 // 32, 1024),
+                                  (oracle.MXFP8, 1024 // 128, 1024)):
+        N = 256
+        ids = np.arange(N * cols_per_row, dtype=np.int64)
+        for byte in range(2):   # unique 16-bit ids, one byte at a time
+            sf = ((ids >> (8 * byte)) & 255).astype(np.uint8).reshape(N, cols_per_row)
+            img = oracle.sf_image(mode, sf, N, K)
+            if byte == 0:
+                lo = img.astype(np.int64)
+            else:
+                hi = img.astype(np.int64)
+        got = np.sort(lo | (hi << 8))
+        reps = 4 if mode == oracle.MXFP8 else 1
+        assert np.array_equal(got, np.sort(np.repeat(ids, reps)))
