@@ -185,7 +185,10 @@ FG_API fg_status fg_gemm_plan(int mode, int64_t M, int64_t N, int64_t K, int spl
  * this shape and split: 0 when the split resolves to 1 or to at most 8 (the
  * splits of a tile then reduce inside one thread-block cluster, with no
  * global scratch), split_k*M*N*4 for larger splits, and the A scale image
- * for large-M MX shapes.  A call with FG_FLAG_DEFER_REDUCE always needs
+ * for large-M MX shapes.  For large-M bf16 / fp8 shapes whose tiles leave a
+ * partial last wave it is the optional stream-K workspace (fp32 partial
+ * tiles of the CTAs that split a tile): with less, those shapes still run,
+ * every tile whole.  A call with FG_FLAG_DEFER_REDUCE always needs
  * split_k*M*N*4 bytes.
  */
 FG_API fg_status fg_gemm_workspace_size(int mode, int64_t M, int64_t N, int64_t K, int split_k, uint64_t* bytes);

@@ -17,6 +17,7 @@
 #include <cstdio>
 #include <cstdlib>
 #include <cstring>
+#include <ctime>
 #include <mutex>
 
 #include "../../include/fg.h"
@@ -224,6 +225,36 @@ fg_status make_plan(int mode, int64_t M, int64_t N, int64_t K, int split_k, fg_p
   return FG_OK;
 }
 
+// Stream-K tail of the large-M bf16 / fp8 kernel: used when the tile count
+// leaves a partial last wave.  Fills the schedule fields of p; returns the
+// workspace bytes it needs (0 = every tile is processed whole).
+uint64_t large_streamk_plan(int mode, int64_t tiles, int64_t KB, int ctas, LargeParams* p) {
+  if (p) {
+    p->dp_rounds = 0;
+    p->dp_tiles = 0;
+    p->sk_iters = 0;
+  }
+  if (is_mx(mode) || ctas <= 0 || tiles <= ctas || tiles % ctas == 0) return 0;
+  const int64_t full_waves = tiles / ctas;
+  const int64_t dp_rounds = full_waves - 1;
+  const int64_t sk_tiles = tiles - dp_rounds * ctas;  // >= ctas: every CTA range spans >= one tile of K
+  if (p) {
+    p->dp_rounds = static_cast<int>(dp_rounds);
+    p->dp_tiles = static_cast<int>(dp_rounds * ctas);
+    p->sk_iters = sk_tiles * KB;
+  }
+  return large_streamk_bytes(ctas);
+}
+
+// A 64-bit tag per launch: a stream-K flag matches only the launch that
+// wrote it (workspace contents from earlier calls never do).
+uint64_t next_epoch() {
+  static std::atomic<uint64_t> counter{0};
+  static const uint64_t salt = (static_cast<uint64_t>(reinterpret_cast<uintptr_t>(&counter)) * 0x9E3779B97F4A7C15ull) ^
+                               (static_cast<uint64_t>(time(nullptr)) << 32);
+  return salt + 2 * (counter.fetch_add(1) + 1);
+}
+
 // ---------------------------------------------------------- TMA set-up
 
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
@@ -407,8 +438,11 @@ fg_status fg_gemm_workspace_size(int mode, int64_t M, int64_t N, int64_t K, int 
   fg_plan plan;
   fg_status s = fg_gemm_plan(mode, M, N, K, split_k, &plan);
   if (s != FG_OK) return s;
-  if (plan.path == 1)
-    *bytes = is_mx(mode) ? sf_rows_image_bytes(mode, M, K) : 0;
+  if (plan.path == 1) {
+    const int64_t tiles = ((M + 127) / 128) * (N / 256 + (N % 256 ? 1 : 0));
+    *bytes = is_mx(mode) ? sf_rows_image_bytes(mode, M, K)
+                         : large_streamk_plan(mode, tiles, row_bytes(mode, K) / 128, plan.ctas, nullptr);
+  }
   else
     *bytes = plan.split_k > kMaxClusterSplit ? static_cast<uint64_t>(plan.split_k) * M * N * 4 : 0;
   return FG_OK;
@@ -480,6 +514,18 @@ fg_status fg_gemm(const void* A, const void* a_scales, int64_t M, const fg_bshuf
     p.tiles_m = static_cast<int>((M + 127) / 128);
     p.tiles_n = static_cast<int>(N / 256 + (N % 256 ? 1 : 0));
     p.debug_stall = (flags & FG_FLAG_DEBUG_STALL) ? 1 : 0;
+    if (!mx) {
+      // the stream-K tail is an optimisation: only with a large enough workspace
+      const uint64_t need = large_streamk_plan(mode, static_cast<int64_t>(p.tiles_m) * p.tiles_n, p.KB, plan.ctas, &p);
+      if (need && workspace && workspace_bytes >= need && aligned(workspace, 16)) {
+        p.sk_part = static_cast<float*>(workspace);
+        p.sk_flag = reinterpret_cast<unsigned long long*>(static_cast<uint8_t*>(workspace) +
+                                                           need - static_cast<uint64_t>(plan.ctas) * 32);
+        p.epoch = next_epoch();
+      } else {
+        large_streamk_plan(mode, 0, 0, 0, &p);  // all tiles whole
+      }
+    }
     if (mx) {
       e = launch_relayout_sf_rows(mode, static_cast<const uint8_t*>(a_scales), static_cast<uint8_t*>(workspace), M, K,
                                   st);

@@ -57,7 +57,21 @@ struct LargeParams {
   int KB;
   int tiles_m, tiles_n;
   int debug_stall;
+  // Stream-K tail (bf16 / fp8 per-tensor; sk_iters == 0: all tiles whole).
+  // Each CTA first takes dp_rounds whole tiles (c, c + G, ...), then an equal
+  // contiguous range of the remaining K iterations.  A tile split between
+  // CTAs c and c+1 is finished by c (which holds its first iterations and
+  // reaches them last) after c+1 published its fp32 partial.
+  int dp_rounds;
+  int dp_tiles;
+  long long sk_iters;
+  float* sk_part;                  // [G][256 columns][128 rows] fp32
+  unsigned long long* sk_flag;     // [G][4 warps]: equals `epoch` once published
+  unsigned long long epoch;
 };
+
+// Bytes of the optional stream-K workspace of the large-M bf16 / fp8 kernel.
+uint64_t large_streamk_bytes(int ctas);
 
 bool decode_config_supported(const DecodeConfig& c);
 // Kernels are launched with programmatic dependent launch (they may start

@@ -18,6 +18,13 @@
 // Tile order: tiles are walked in groups of `group_n` weight tiles; inside a
 // group the weight tile index runs fastest, so the CTAs resident at one time
 // share a band of weights (kept in L2) and a few A row blocks.
+//
+// Stream-K tail (bf16 / fp8, when the caller gives the workspace): when the
+// tile count is not a multiple of the CTA count, the last partial wave would
+// leave most SMs idle.  Instead each CTA takes its whole tiles for all but
+// the last full wave, then an equal contiguous range of the remaining K
+// iterations; a tile split between CTAs c and c+1 is finished by c after c+1
+// published its fp32 partial (cooperative launch, bounded waits).
 #include <cuda_bf16.h>
 
 #include "fg_internal.cuh"
@@ -58,6 +65,34 @@ __device__ __forceinline__ TileCoord tile_coord(int t, int tiles_m, int tiles_n)
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   const __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
   return *reinterpret_cast<const uint32_t*>(&v);
+}
+
+// One unit of a CTA's work: K iterations [k0, k1) of tile t.
+struct Chunk {
+  int t, k0, k1;
+};
+
+__device__ __forceinline__ int chunk_count(const LargeParams& p, int c, int G, int tiles, int KB) {
+  if (p.sk_iters == 0) return c < tiles ? (tiles - c + G - 1) / G : 0;
+  const long long s = p.sk_iters * c / G, e = p.sk_iters * (c + 1) / G;
+  return p.dp_rounds + (e > s ? static_cast<int>((e - 1) / KB - s / KB + 1) : 0);
+}
+
+__device__ __forceinline__ Chunk chunk_at(const LargeParams& p, int c, int G, int KB, int i) {
+  Chunk ch;
+  if (p.sk_iters == 0 || i < p.dp_rounds) {
+    ch.t = c + i * G;
+    ch.k0 = 0;
+    ch.k1 = KB;
+    return ch;
+  }
+  const long long s = p.sk_iters * c / G, e = p.sk_iters * (c + 1) / G;
+  const int j = i - p.dp_rounds;
+  const long long tf = s / KB + j;
+  ch.t = p.dp_tiles + static_cast<int>(tf);
+  ch.k0 = j == 0 ? static_cast<int>(s - tf * KB) : 0;
+  ch.k1 = static_cast<int>(e - tf * KB < KB ? e - tf * KB : KB);
+  return ch;
 }
 
 template <int MODE>
@@ -110,10 +145,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       int it = 0;
       bool ok = true;
-      for (int t = blockIdx.x; ok && t < tiles; t += gridDim.x) {
-        const TileCoord tc = tile_coord(t, p.tiles_m, p.tiles_n);
+      const int nch = chunk_count(p, blockIdx.x, gridDim.x, tiles, KB);
+      for (int ci = 0; ok && ci < nch; ++ci) {
+        const Chunk ch = chunk_at(p, blockIdx.x, gridDim.x, KB, ci);
+        const TileCoord tc = tile_coord(ch.t, p.tiles_m, p.tiles_n);
         const int nslabs_n = min(2, p.N / 128 - 2 * tc.n);  // weight slabs in this tile (1 or 2)
-        for (int kb = 0; kb < KB; ++kb, ++it) {
+        for (int kb = ch.k0; kb < ch.k1; ++kb, ++it) {
           const int slot = it % kStages;
           if (!mbar_wait(&empty_bar[slot], ((it / kStages) & 1) ^ 1u, T, p.err, 11)) {
             ok = false;
@@ -137,7 +174,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (p.debug_stall) ok = mbar_wait(&stall_bar, 0, T, p.err, 12);
       int it = 0, ti = 0;
       const uint32_t idesc = MODE == kBF16 ? idesc_bf16(kBM, kBN) : idesc_e4m3(kBM, kBN);
-      for (int t = blockIdx.x; ok && t < tiles; t += gridDim.x, ++ti) {
+      const int nch = chunk_count(p, blockIdx.x, gridDim.x, tiles, KB);
+      for (; ok && ti < nch; ++ti) {
+        const Chunk ch = chunk_at(p, blockIdx.x, gridDim.x, KB, ti);
         const int acc = ti & 1;
         if (!mbar_wait(&acce_bar[acc], ((ti >> 1) & 1) ^ 1u, T, p.err, 13)) {
           ok = false;
@@ -145,7 +184,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         tc_fence_after();
         const uint32_t d = tmem + acc * kBN;
-        for (int kb = 0; kb < KB; ++kb, ++it) {
+        for (int kb = ch.k0; kb < ch.k1; ++kb, ++it) {
           const int slot = it % kStages;
           if (!mbar_wait(&full_bar[slot], (it / kStages) & 1, T, p.err, 14)) {
             ok = false;
@@ -158,10 +197,11 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int j = 0; j < 4; ++j) {
             const uint64_t adesc = sdesc_sw128(smem_u32(st + j * 32));
             const uint64_t bdesc = sdesc_sw128(smem_u32(st + kABytes + j * 32));
+            const uint32_t accum = (kb > ch.k0 || j > 0) ? 1u : 0u;
             if (MODE == kBF16)
-              mma_f16(d, adesc, bdesc, idesc, (kb | j) != 0);
+              mma_f16(d, adesc, bdesc, idesc, accum);
             else
-              mma_f8f6f4(d, adesc, bdesc, idesc, (kb | j) != 0);
+              mma_f8f6f4(d, adesc, bdesc, idesc, accum);
           }
           tc_commit(&empty_bar[slot]);
         }
@@ -183,8 +223,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int qd = warp & 3;
     float scale = 1.f;
     if (MODE == kTensor) scale = __ldg(static_cast<const float*>(p.a_scales)) * __ldg(p.b_s);
-    int ti = 0;
-    for (int t = blockIdx.x; t < tiles; t += gridDim.x, ++ti) {
+    const int nch = chunk_count(p, blockIdx.x, gridDim.x, tiles, KB);
+    for (int ti = 0; ti < nch; ++ti) {
+      const Chunk ch = chunk_at(p, blockIdx.x, gridDim.x, KB, ti);
       const int acc = ti & 1;
       const bool w = mbar_wait(&accf_bar[acc], (ti >> 1) & 1, T, p.err, 16);
       if (!__all_sync(0xffffffffu, w)) {
@@ -192,25 +233,60 @@ __global__ void __launch_bounds__(kThreads, 1)
         break;
       }
       tc_fence_after();
-      const TileCoord tc = tile_coord(t, p.tiles_m, p.tiles_n);
-      const int row = tc.m * kBM + qd * 32 + lane;
+      const TileCoord tc = tile_coord(ch.t, p.tiles_m, p.tiles_n);
+      const int lrow = qd * 32 + lane;
+      const int row = tc.m * kBM + lrow;
       const int ncols = min(kBN, p.N - tc.n * kBN);
-      __nv_bfloat16* yrow = p.y + static_cast<size_t>(row) * p.N + static_cast<size_t>(tc.n) * kBN;
       const uint32_t taddr = tmem + acc * kBN + (static_cast<uint32_t>(qd * 32) << 16);
-      for (int c = 0; c < ncols; c += 32) {
-        uint32_t v[32];
-        tmem_ld32(taddr + c, v);
-        tmem_wait_ld();
-        if (row < p.M) {
-          uint4* dst = reinterpret_cast<uint4*>(yrow + c);
+      if (ch.k0 > 0) {
+        // Stream-K: this CTA holds the last iterations of the tile; publish
+        // the raw fp32 partial ([column][row], this warp's 32 rows) for the
+        // CTA that finishes the tile.
+        float* part = p.sk_part + static_cast<size_t>(blockIdx.x) * kBN * kBM;
+        for (int c = 0; c < kBN; c += 32) {
+          uint32_t v[32];
+          tmem_ld32(taddr + c, v);
+          tmem_wait_ld();
 #pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            uint4 o;
-            o.x = pack_bf16x2(__uint_as_float(v[8 * q + 0]) * scale, __uint_as_float(v[8 * q + 1]) * scale);
-            o.y = pack_bf16x2(__uint_as_float(v[8 * q + 2]) * scale, __uint_as_float(v[8 * q + 3]) * scale);
-            o.z = pack_bf16x2(__uint_as_float(v[8 * q + 4]) * scale, __uint_as_float(v[8 * q + 5]) * scale);
-            o.w = pack_bf16x2(__uint_as_float(v[8 * q + 6]) * scale, __uint_as_float(v[8 * q + 7]) * scale);
-            dst[q] = o;
+          for (int i = 0; i < 32; ++i) __stcg(part + (c + i) * kBM + lrow, __uint_as_float(v[i]));
+        }
+        __threadfence();
+        __syncwarp();
+        if (lane == 0) st_release_u64(p.sk_flag + blockIdx.x * 4 + qd, p.epoch);
+      } else {
+        const bool finish = ch.k1 < KB;  // the rest of the tile comes from CTA blockIdx.x + 1
+        const float* peer = p.sk_part + static_cast<size_t>(blockIdx.x + 1) * kBN * kBM;
+        bool have_peer = true;
+        if (finish) {
+          bool fw = true;
+          if (lane == 0) fw = wait_flag_eq(p.sk_flag + (blockIdx.x + 1) * 4 + qd, p.epoch, T, p.err, 17);
+          have_peer = __shfl_sync(0xffffffffu, fw ? 1 : 0, 0) != 0;
+          if (have_peer) (void)ld_acquire_u64(p.sk_flag + (blockIdx.x + 1) * 4 + qd);
+          else if (lane == 0) abort_sh = 1;
+        }
+        __nv_bfloat16* yrow = p.y + static_cast<size_t>(row) * p.N + static_cast<size_t>(tc.n) * kBN;
+        for (int c = 0; c < ncols; c += 32) {
+          uint32_t v[32];
+          tmem_ld32(taddr + c, v);
+          tmem_wait_ld();
+          float f[32];
+#pragma unroll
+          for (int i = 0; i < 32; ++i) f[i] = __uint_as_float(v[i]);
+          if (finish && have_peer) {
+#pragma unroll
+            for (int i = 0; i < 32; ++i) f[i] += __ldcg(peer + (c + i) * kBM + lrow);
+          }
+          if (row < p.M && have_peer) {
+            uint4* dst = reinterpret_cast<uint4*>(yrow + c);
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+              uint4 o;
+              o.x = pack_bf16x2(f[8 * q + 0] * scale, f[8 * q + 1] * scale);
+              o.y = pack_bf16x2(f[8 * q + 2] * scale, f[8 * q + 3] * scale);
+              o.z = pack_bf16x2(f[8 * q + 4] * scale, f[8 * q + 5] * scale);
+              o.w = pack_bf16x2(f[8 * q + 6] * scale, f[8 * q + 7] * scale);
+              dst[q] = o;
+            }
           }
         }
       }
@@ -240,8 +316,17 @@ cudaError_t launch_mode(const CUtensorMap& tmap_a, const LargeParams& p, int cta
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
-  large_kernel<MODE><<<ctas, kThreads, kSmem, stream>>>(tmap_a, p);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(ctas);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = kSmem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr;
+  attr.id = cudaLaunchAttributeCooperative;  // stream-K CTAs wait on one another: all must be resident
+  attr.val.cooperative = 1;
+  cfg.attrs = &attr;
+  cfg.numAttrs = p.sk_iters > 0 ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, large_kernel<MODE>, tmap_a, p);
 }
 
 
@@ -465,6 +550,10 @@ cudaError_t launch_mx(const CUtensorMap& tmap_a, const LargeParams& p, int ctas,
 }
 
 }  // namespace
+
+uint64_t large_streamk_bytes(int ctas) {
+  return static_cast<uint64_t>(ctas) * (static_cast<uint64_t>(kBN) * kBM * 4 + 4 * 8);
+}
 
 bool large_supported(int mode) { return mode == kBF16 || mode == kTensor || is_mx(mode); }
 

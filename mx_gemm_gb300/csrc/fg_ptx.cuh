@@ -277,6 +277,33 @@ __device__ __forceinline__ void pdl_launch_dependents() {
 
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 
+// ------------------------------------------------- flags between CTAs
+
+__device__ __forceinline__ void st_release_u64(unsigned long long* p, unsigned long long v) {
+  asm volatile("st.release.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
+}
+
+__device__ __forceinline__ unsigned long long ld_acquire_u64(const unsigned long long* p) {
+  unsigned long long v;
+  asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+  return v;
+}
+
+// Wait until *flag == want (another CTA of the same cooperative launch
+// publishes it with st_release_u64); bounded like mbar_wait.
+__device__ __forceinline__ bool wait_flag_eq(const unsigned long long* flag, unsigned long long want,
+                                             uint64_t timeout_ns, uint32_t* err, uint32_t where) {
+  const uint64_t t0 = globaltimer_ns();
+  while (ld_acquire_u64(flag) != want) {
+    if (globaltimer_ns() - t0 > timeout_ns) {
+      if (err) atomicCAS(err, 0u, kDevErrTimeout | (where << 8));
+      return false;
+    }
+    __nanosleep(64);
+  }
+  return true;
+}
+
 // ------------------------------------------------------------- descriptors
 
 // Shared-memory matrix descriptor for a K-major operand stored in the

@@ -66,3 +66,27 @@ def test_large_workload_parity_sampled_rows(mode, M, N, K, name, idx):
     ref = c.ref(rows=rows)
     parity.assert_y_close(y, ref, f"{mode} {M}x{N}x{K} sampled rows")
     assert fg.get_error() == fg.FG_OK
+
+
+@pytest.mark.parametrize("mode", ["bf16", "fp8_tensor"])
+def test_streamk_tail_matches_whole_tiles(mode):
+    """160 tiles on the GPU's CTAs leave a partial wave: with the workspace
+    the tail runs stream-K (tiles split between CTAs, fp32 partials passed
+    between them); without it every tile runs whole.  Both match the oracle."""
+    M, N, K = 2560, 2048, 2048
+    c = Case(mode, *inputs.operands(mode, M, N, K, 91, 92, 93))
+    need = fg.gemm_workspace_size(mode, M, N, K)
+    assert need > 0
+    rows = inputs.sample_rows(M)
+    ref = c.ref(rows=rows)
+    idx = torch.from_numpy(rows).cuda()
+    ws = torch.empty(need // 4, dtype=torch.float32, device="cuda")
+    y_sk = c.gemm(workspace=ws)
+    y_whole = c.gemm(workspace=torch.empty(4, dtype=torch.float32, device="cuda"))
+    parity.assert_y_close(y_to_f64(y_sk[idx]), ref, f"{mode} stream-K")
+    parity.assert_y_close(y_to_f64(y_whole[idx]), ref, f"{mode} whole tiles")
+    parity.assert_y_close(y_to_f64(y_sk), y_to_f64(y_whole), f"{mode} stream-K vs whole")
+    # a second call with the same workspace (flags from the first call must not be mistaken)
+    y_sk2 = c.gemm(workspace=ws)
+    assert torch.equal(y_sk.view(torch.int16), y_sk2.view(torch.int16))
+    assert fg.get_error() == fg.FG_OK
