@@ -90,3 +90,29 @@ def test_streamk_tail_matches_whole_tiles(mode):
     y_sk2 = c.gemm(workspace=ws)
     assert torch.equal(y_sk.view(torch.int16), y_sk2.view(torch.int16))
     assert fg.get_error() == fg.FG_OK
+
+
+@pytest.mark.parametrize("mode,M,N,K,streamk", [
+    ("fp8_tensor", 2560, 2048, 1024, True),    # stream-K tail: cooperative CTAs that wait on one another
+    ("bf16", 300, 512, 1024, False),
+    ("mxfp4", 300, 512, 1024, False),
+])
+def test_large_bounded_wait_reports_timeout(mode, M, N, K, streamk):
+    """The MMA issuer waits on a barrier nothing arrives at: every wait of the
+    large-M kernels runs out after the limit, the kernel drains what it
+    started and returns, the host reads FG_ERR_TIMEOUT, and a normal call
+    afterwards is correct."""
+    c = Case(mode, *inputs.operands(mode, M, N, K, 81, 82, 83))
+    assert fg.get_error() == fg.FG_OK
+    ws = torch.empty(max(4, fg.gemm_workspace_size(mode, M, N, K)) // 4, dtype=torch.float32, device="cuda")
+    assert (fg.gemm_workspace_size(mode, M, N, K) > 0) == (streamk or mode == "mxfp4")
+    fg.set_wait_timeout_ns(20_000_000)
+    try:
+        c.gemm(workspace=ws, flags=fg.FG_FLAG_DEBUG_STALL)
+        assert fg.get_error() == fg.FG_ERR_TIMEOUT
+    finally:
+        fg.set_wait_timeout_ns(4_000_000_000)
+    assert fg.get_error() == fg.FG_OK
+    rows = inputs.sample_rows(M, n=64)
+    y = c.gemm(workspace=ws)
+    parity.assert_y_close(y_to_f64(y[torch.from_numpy(rows).cuda()]), c.ref(rows=rows), f"{mode} after timeout")
