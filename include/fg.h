@@ -263,7 +263,12 @@ FG_API fg_status fg_gemm_noalloc(const void* A, const void* a_scales, int64_t M,
  */
 FG_API fg_status fg_get_error(void);
 
-/* Limit for every wait inside the kernels, in nanoseconds (default 4e9). */
+/*
+ * Limit for every wait inside the kernels, in nanoseconds (default 4e9).
+ * Values below 1e6 (1 ms) are raised to 1 ms: a wait that gives up must not
+ * end while the cluster peers' shared-memory stores it waits for (a few
+ * microseconds apart) may still be on their way.
+ */
 FG_API void fg_set_wait_timeout_ns(uint64_t ns);
 
 /*

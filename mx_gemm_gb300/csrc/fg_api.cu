@@ -335,7 +335,7 @@ const char* fg_status_str(int s) {
 
 const char* fg_last_error_message(void) { return g_msg; }
 
-void fg_set_wait_timeout_ns(uint64_t ns) { g_timeout_ns.store(ns ? ns : 1); }
+void fg_set_wait_timeout_ns(uint64_t ns) { g_timeout_ns.store(ns < 1000000 ? 1000000 : ns); }
 
 void fg_debug_override_cc(int major, int minor) {
   g_cc_minor_override.store(minor);

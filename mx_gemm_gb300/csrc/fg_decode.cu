@@ -30,13 +30,20 @@
 //             splits within the workspace bound.
 //
 // Split-K reduction: with split > 1 the S split CTAs of a tile run as one
-// thread-block cluster.  Each writes its fp32 partial [16 tokens][128 rows]
-// into its own shared memory; after a cluster barrier, CTA r sums rows
-// [r*128/S, (r+1)*128/S) over the S partials through distributed shared
-// memory in split order 0..S-1 (the order of the two-pass reduce, so both
-// paths give the same bits), applies the per-tensor scale and stores bf16.
-// The two-pass form (fp32 workspace + reduce kernel) remains for
-// FG_FLAG_DEFER_REDUCE and for splits beyond the cluster size limit.
+// thread-block cluster, and CTA r owns rows [ceil(128 r/S), ceil(128 (r+1)/S))
+// of the tile.  Each CTA's receive area is the stage buffer its last
+// iterations leave idle first; once the MMAs that read that buffer are done,
+// the producer thread tells every peer so (one remote mbarrier arrival each).
+// When a CTA's fp32 partial [128 rows][16 tokens] is in registers and all
+// peers are ready, its epilogue threads store each row's tokens straight into
+// the owner's receive area (st.async, 16 bytes at a time, counted on the
+// owner's mbarrier).  The owner then sums its rows over the S slices in split
+// order 0..S-1 (the order of the two-pass reduce, so both paths give the same
+// bits), applies the per-tensor scale and stores bf16.  A cluster barrier
+// split into arrive (after a CTA has received everything) and wait (at exit)
+// keeps every CTA alive until all stores into it have landed.  The two-pass
+// form (fp32 workspace + reduce kernel) remains for FG_FLAG_DEFER_REDUCE and
+// for splits beyond the cluster size limit.
 //
 // Launch order: every launch allows the next kernel of the stream to start
 // early (programmatic dependent launch).  The producer streams its first
@@ -105,6 +112,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   __shared__ __align__(8) uint64_t pfull_bar[C::NBUF];
   __shared__ __align__(8) uint64_t pempty_bar[C::NBUF];
   __shared__ __align__(8) uint64_t acc_bar, stall_bar, drain_bar;
+  __shared__ __align__(8) uint64_t ready_bar, recv_bar;  // fused split-K reduce
   __shared__ uint32_t tmem_base_sh;
   __shared__ int abort_sh, issued_sh, consumed_sh, mma_any_sh;
 
@@ -115,6 +123,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int nslab = q + (split < r ? 1 : 0);
   const int niter = (nslab + SPS - 1) / SPS;
   const uint64_t T = p.timeout_ns;
+  // fused reduce: the stage buffer that holds split s's receive area
+  auto recv_slot = [&](int s) {
+    const int ns = q + (s < r ? 1 : 0);
+    return ((ns + SPS - 1) / SPS) % STAGES;
+  };
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < STAGES; ++i) {
@@ -128,6 +141,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(&acc_bar, 1);
     mbar_init(&stall_bar, 1);
     mbar_init(&drain_bar, 1);
+    mbar_init(&ready_bar, p.split > 1 ? p.split - 1 : 1);
+    mbar_init(&recv_bar, 1);
     abort_sh = 0;
     issued_sh = 0;
     consumed_sh = 0;
@@ -142,6 +157,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
+  // phase 1 of the cluster barrier: waited on before the first access to a
+  // peer, it guarantees the peer's mbarriers are initialised
+  if (p.fused_reduce) cluster_arrive_relaxed();
   const uint32_t tmem = tmem_base_sh;
   if (threadIdx.x == 0) pdl_launch_dependents();
 
@@ -196,6 +214,28 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     if (it < pre) pdl_wait();  // aborted before the prefetch window closed
     if (lane == 0) issued_sh = it;
+    __syncwarp();
+    if (p.fused_reduce) {
+      cluster_wait();  // phase 1
+      if (lane == 0) {
+        // The receive area lives in stage buffer niter % STAGES, idle once the
+        // MMAs of the last iteration that used it (niter - STAGES) are done.
+        // After an abort (it < niter) the signal goes out at once; the peers
+        // then run out of time waiting for data that never comes.
+        const int itf = niter - STAGES;
+        if (itf >= 0 && it == niter) mbar_wait(&empty_bar[niter % STAGES], (itf / STAGES) & 1, T, p.err, 9);
+        const int S = p.split;
+        const int Mt = min(kTokRows, p.M - mt * kTokRows);
+        const int myR = (128 * (split + 1) + S - 1) / S - (128 * split + S - 1) / S;
+        mbar_arrive_expect_tx(&recv_bar, static_cast<uint32_t>((S - 1) * myR * ((Mt + 3) / 4) * 16));
+        for (int s2 = 0; s2 < S; ++s2)
+          if (s2 != split) mbar_arrive_remote(&ready_bar, s2);
+      }
+      __syncwarp();
+      // phase 2; the release keeps it behind the arrivals just sent to the
+      // peers, so no peer can leave before they have landed
+      cluster_arrive();
+    }
   } else if (warp == 1) {
     // ---------------------------------------------------------- MMA issuer
     if (lane == 0) {
@@ -272,6 +312,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_wait(&drain_bar, 0, T, p.err, 7);
       }
     }
+    __syncwarp();
+    if (p.fused_reduce) {
+      cluster_wait();            // phase 1
+      cluster_arrive_relaxed();  // phase 2 (this warp stores nothing into peers)
+    }
   } else {
     // ------------------------------------------------------------ epilogue
     if (C::APS) {
@@ -317,6 +362,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!okb && lane == 0) abort_sh = 1;
     }
     pdl_wait();
+    // per-tensor output scale, loaded long before it is needed
+    const float out_scale = MODE == kTensor ? __ldg(static_cast<const float*>(p.a_scales)) * __ldg(p.b_s) : 1.f;
     const int qd = warp & 3;
     const int nrow = nt * 128 + qd * 32 + lane;
     const uint32_t trow = tmem + (static_cast<uint32_t>(qd * 32) << 16);
@@ -376,26 +423,66 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int m = 0; m < kTokRows; ++m) acc[m] = __uint_as_float(v[m]);
       }
     }
-    if (!ok) {
-      if (lane == 0) abort_sh = 1;
-    } else if (p.fused_reduce) {
-      // partial [token m][local row] into this CTA's (now idle) stage memory
-      float* part = reinterpret_cast<float*>(smem);
+    if (!ok && lane == 0) abort_sh = 1;
+    if (p.fused_reduce) {
+      // Receive area of split s2: fp32 [S][RM][MV][4], slice s, local row j,
+      // tokens 4v..4v+3 (tokens >= Mt are the zero rows of the token tile).
+      const int S = p.split;
+      const int RM = (128 + S - 1) / S;
+      const int Mt = min(kTokRows, p.M - mt * kTokRows);
+      const int MV = (Mt + 3) / 4;
+      const int lr = qd * 32 + lane;
+      const int owner = lr * S / 128;
+      const int j = lr - (128 * owner + S - 1) / S;
+      cluster_wait();  // phase 1
+      const bool rd = mbar_wait_cluster<false>(&ready_bar, 0, T, p.err, 10);
+      if (ok && rd) {
+        float* dst = reinterpret_cast<float*>(smem + recv_slot(owner) * C::STAGE_BYTES) +
+                     ((split * RM + j) * MV) * 4;
 #pragma unroll
-      for (int m = 0; m < kTokRows; ++m) part[m * 128 + qd * 32 + lane] = acc[m];
-    } else if (p.split > 1) {
+        for (int v = 0; v < 4; ++v) {
+          if (v < MV) {
+            const float4 val = make_float4(acc[4 * v], acc[4 * v + 1], acc[4 * v + 2], acc[4 * v + 3]);
+            if (owner == split)
+              *reinterpret_cast<float4*>(dst + 4 * v) = val;
+            else
+              st_async_f32x4(dst + 4 * v, owner, val, &recv_bar);
+          }
+        }
+      }
+      const bool rv = mbar_wait_cluster<true>(&recv_bar, 0, T, p.err, 11);
+      cluster_arrive_relaxed();  // phase 2: everything bound for this CTA has landed
+      bar_sync_named(1, 128);   // this CTA's own slice, written by all four warps
+      if (ok && rd && rv) {
+        const int rlo = (128 * split + S - 1) / S;
+        const int myR = (128 * (split + 1) + S - 1) / S - rlo;
+        const float* rbuf = reinterpret_cast<const float*>(smem + recv_slot(split) * C::STAGE_BYTES);
+        const int et = threadIdx.x - 64;
+        for (int e = et; e < myR * MV; e += 128) {
+          const int jj = e % myR, v = e / myR;
+          float4 a = *reinterpret_cast<const float4*>(rbuf + (jj * MV + v) * 4);
+          for (int s2 = 1; s2 < S; ++s2) {
+            const float4 b = *reinterpret_cast<const float4*>(rbuf + ((s2 * RM + jj) * MV + v) * 4);
+            a.x += b.x; a.y += b.y; a.z += b.z; a.w += b.w;
+          }
+          const float av[4] = {a.x, a.y, a.z, a.w};
+          __nv_bfloat16* yc = p.y + static_cast<size_t>(mt * kTokRows + 4 * v) * p.N + nt * 128 + rlo + jj;
+#pragma unroll
+          for (int c = 0; c < 4; ++c)
+            if (4 * v + c < Mt) yc[static_cast<size_t>(c) * p.N] = __float2bfloat16_rn(av[c] * out_scale);
+        }
+      }
+    } else if (ok && p.split > 1) {
 #pragma unroll
       for (int m = 0; m < kTokRows; ++m) {
         const int row = mt * kTokRows + m;
         if (row < p.M) p.ws[(static_cast<size_t>(split) * p.M + row) * p.N + nrow] = acc[m];
       }
-    } else {
-      float scale = 1.f;
-      if (MODE == kTensor) scale = __ldg(static_cast<const float*>(p.a_scales)) * __ldg(p.b_s);
+    } else if (ok) {
 #pragma unroll
       for (int m = 0; m < kTokRows; ++m) {
         const int row = mt * kTokRows + m;
-        if (row < p.M) p.y[static_cast<size_t>(row) * p.N + nrow] = __float2bfloat16_rn(acc[m] * scale);
+        if (row < p.M) p.y[static_cast<size_t>(row) * p.N + nrow] = __float2bfloat16_rn(acc[m] * out_scale);
       }
     }
   }
@@ -403,38 +490,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   // ------------------------------------------------------------- teardown
   tc_fence_before();
   __syncthreads();
-  if (p.fused_reduce) {
-    // Every thread of every CTA of the cluster passes both barriers, on the
-    // normal and on the abort path alike.
-    cluster_sync();  // all partials of the tile are in place
-    const int et = static_cast<int>(threadIdx.x) - 64;
-    if (!abort_sh && et >= 0) {
-      const int S = p.split;
-      const int R = 128 / S;          // rows this CTA reduces
-      const int r0 = split * R;
-      float scale = 1.f;
-      if (MODE == kTensor) scale = __ldg(static_cast<const float*>(p.a_scales)) * __ldg(p.b_s);
-      const float* part = reinterpret_cast<const float*>(smem);
-      for (int e = et; e < kTokRows * R / 4; e += 128) {
-        const int m = e / (R / 4);
-        const int lr = r0 + (e % (R / 4)) * 4;
-        const int row = mt * kTokRows + m;
-        if (row >= p.M) continue;
-        float4 a = ld_dsmem_f32x4(part + m * 128 + lr, 0);
-        for (int s2 = 1; s2 < S; ++s2) {
-          const float4 v = ld_dsmem_f32x4(part + m * 128 + lr, s2);
-          a.x += v.x; a.y += v.y; a.z += v.z; a.w += v.w;
-        }
-        const __nv_bfloat162 lo = __floats2bfloat162_rn(a.x * scale, a.y * scale);
-        const __nv_bfloat162 hi = __floats2bfloat162_rn(a.z * scale, a.w * scale);
-        uint2 o;
-        o.x = *reinterpret_cast<const uint32_t*>(&lo);
-        o.y = *reinterpret_cast<const uint32_t*>(&hi);
-        *reinterpret_cast<uint2*>(p.y + static_cast<size_t>(row) * p.N + nt * 128 + lr) = o;
-      }
-    }
-    cluster_sync();  // no CTA leaves while a peer may still read its partial
-  }
   if (abort_sh) {
     // Let every copy this CTA started land before its shared memory goes
     // away, and every MMA it issued finish before TMEM is released.
@@ -446,6 +501,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   if (warp == 1) tmem_dealloc(tmem, C::TMEM_COLS);
+  if (p.fused_reduce) cluster_wait();  // phase 2: no peer stores into this CTA any more
 }
 
 template <int MODE, int SPS, int STAGES>

@@ -208,25 +208,92 @@ __device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.
 
 // ------------------------------------------------- clusters and launch order
 
-// Every thread of every CTA of the cluster must execute this, the same number
-// of times; the library's kernels only call it on paths all threads take.
-__device__ __forceinline__ void cluster_sync() {
-  asm volatile(
-      "barrier.cluster.arrive.release.aligned;\n"
-      "barrier.cluster.wait.acquire.aligned;" ::: "memory");
+// Cluster barrier, split into its two halves.  Every thread of every CTA of
+// the cluster arrives and then waits, alternately, the same number of times;
+// the library's kernels call them on paths whole warps take.  The relaxed
+// arrive orders none of the thread's memory operations: it serves where the
+// barrier only has to say "this thread got here" (after fence_mbar_init,
+// whose own release publishes the barrier inits, or after a wait that saw
+// everything bound for this CTA land).
+__device__ __forceinline__ void cluster_arrive_relaxed() {
+  asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void cluster_arrive() { asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory"); }
+__device__ __forceinline__ void cluster_wait() { asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory"); }
+
+// Barrier among `count` threads of this CTA (whole warps) on hardware barrier
+// `id` (1..15; 0 is __syncthreads).
+__device__ __forceinline__ void bar_sync_named(uint32_t id, uint32_t count) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
 }
 
-// Load 4 floats from the shared memory of CTA `rank` of this cluster, at the
-// offset `local` has in this CTA's shared memory.
-__device__ __forceinline__ float4 ld_dsmem_f32x4(const void* local, uint32_t rank) {
+// Address in CTA `rank`'s shared memory of the variable at `local` here.
+__device__ __forceinline__ uint32_t mapa_u32(const void* local, uint32_t rank) {
   uint32_t remote;
   asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(smem_u32(local)), "r"(rank));
-  float4 v;
-  asm volatile("ld.shared::cluster.v4.f32 {%0,%1,%2,%3}, [%4];"
-               : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
-               : "r"(remote)
+  return remote;
+}
+
+// One arrival on the mbarrier at `bar`'s offset in CTA `rank` of the cluster.
+// Relaxed: it orders none of this thread's memory operations, so it is only
+// a signal ("a buffer of mine is idle"), never a way to publish data.  (A
+// release at cluster scope here cost microseconds: it waits for the copies
+// still in flight from this SM.)
+__device__ __forceinline__ void mbar_arrive_remote(uint64_t* bar, uint32_t rank) {
+  asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];" ::"r"(mapa_u32(bar, rank))
                : "memory");
-  return v;
+}
+
+// As mbar_wait, for phases completed by other CTAs of the cluster: with
+// ACQUIRE, at cluster scope (the data the phase covers is visible after it);
+// without, relaxed (a pure signal).
+template <bool ACQUIRE>
+__device__ __forceinline__ bool mbar_try_wait_cluster(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  if (ACQUIRE)
+    asm volatile(
+        "{\n .reg .pred p;\n"
+        " mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n"
+        " selp.u32 %0, 1, 0, p;\n}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+  else
+    asm volatile(
+        "{\n .reg .pred p;\n"
+        " mbarrier.try_wait.parity.relaxed.cluster.shared::cta.b64 p, [%1], %2;\n"
+        " selp.u32 %0, 1, 0, p;\n}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+  return ok != 0;
+}
+
+template <bool ACQUIRE>
+__device__ __forceinline__ bool mbar_wait_cluster(uint64_t* bar, uint32_t parity, uint64_t timeout_ns,
+                                                  uint32_t* err, uint32_t where) {
+  if (mbar_try_wait_cluster<ACQUIRE>(bar, parity)) return true;
+  const uint64_t t0 = globaltimer_ns();
+  while (true) {
+#pragma unroll 1
+    for (int i = 0; i < 32; ++i)
+      if (mbar_try_wait_cluster<ACQUIRE>(bar, parity)) return true;
+    if (globaltimer_ns() - t0 > timeout_ns) {
+      if (err) atomicCAS(err, 0u, kDevErrTimeout | (where << 8));
+      return false;
+    }
+  }
+}
+
+// Store 16 bytes from registers into CTA `rank`'s shared memory at `local`'s
+// offset; the store completes 16 bytes of transaction count on that CTA's
+// mbarrier at `bar`'s offset.  `local` 16-byte aligned.
+__device__ __forceinline__ void st_async_f32x4(const void* local, uint32_t rank, float4 v, uint64_t* bar) {
+  asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.b32 [%0], {%1, %2, %3, %4}, [%5];" ::"r"(
+                   mapa_u32(local, rank)),
+               "r"(__float_as_uint(v.x)), "r"(__float_as_uint(v.y)), "r"(__float_as_uint(v.z)),
+               "r"(__float_as_uint(v.w)), "r"(mapa_u32(bar, rank))
+               : "memory");
 }
 
 // Programmatic dependent launch: let the next kernel of the stream start its

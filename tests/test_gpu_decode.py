@@ -51,17 +51,37 @@ def test_split_outputs_agree(mode):
 
 
 @pytest.mark.parametrize("mode", MODES)
-@pytest.mark.parametrize("S", [2, 4, 8])
+@pytest.mark.parametrize("S", [2, 3, 4, 5, 6, 7, 8])
 def test_deferred_reduce_equals_fused_call(mode, S):
     """Two-pass (fp32 workspace + reduce kernel) and the in-cluster reduce sum
-    the same partials in the same order: identical bits."""
+    the same partials in the same order: identical bits, for every cluster
+    size (uneven ones give the CTAs of a tile unequal row counts)."""
     M, N, K = 16, 256, 2048
+    if S > _slabs(mode, K):
+        pytest.skip("more splits than K slabs")
     c = Case(mode, *inputs.operands(mode, M, N, K, 9, 10, 11))
     ws = torch.empty(S * M * N, dtype=torch.float32, device="cuda")
     c.gemm(split_k=S, flags=fg.FG_FLAG_DEFER_REDUCE, workspace=ws)
     y_two = c.reduce(ws, S)
     y_one = c.gemm(split_k=S)
     assert torch.equal(y_two.view(torch.int16), y_one.view(torch.int16))
+
+
+@pytest.mark.parametrize("mode", ["fp8_tensor", "fp8_block128", "mxfp4", "bf16"])
+@pytest.mark.parametrize("S", [3, 5, 6, 7])
+@pytest.mark.parametrize("M", [1, 6, 21])
+def test_fused_uneven_split_matches_oracle(mode, S, M):
+    """Cluster sizes that do not divide the 128 rows of a tile, with ragged
+    token tiles (M = 21: a full tile of 16 and one of 5): every output against
+    the oracle."""
+    N, K = 384, 2048
+    if S > _slabs(mode, K):
+        pytest.skip("more splits than K slabs")
+    c = Case(mode, *inputs.operands(mode, M, N, K, 400 + S, 500 + M, 600))
+    Y = torch.full((M, N), float("nan"), dtype=torch.bfloat16, device="cuda")
+    fg.gemm(c.dA, c.pb, c.da_s, split_k=S, Y=Y)
+    parity.assert_y_close(y_to_f64(Y), c.ref(), f"{mode} M={M} fused split {S}")
+    assert fg.get_error() == fg.FG_OK
 
 
 ONE = {"bf16": 0x3F80, "fp8_tensor": 0x38, "fp8_block128": 0x38, "mxfp8": 0x38, "mxfp4": 0x2,
