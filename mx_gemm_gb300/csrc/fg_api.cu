@@ -136,18 +136,24 @@ struct TableRow {
 };
 
 // Exact-shape rows: the decode shapes of the split-K page (K=7168), each
-// the fastest (split, slabs per stage, stages) of a sweep on GB300 (whole
-// four-GEMM step for the fp8 modes, per shape for MX).  Anything else falls
-// through to the heuristic below.
+// the fastest (split, slabs per stage, stages) of a sweep on GB300 over
+// splits {1,2,4,8} and every instantiated pipeline (per shape: a CUDA graph
+// of back-to-back launches cycling through weight copies larger than twice
+// the L2).  Anything else falls through to the heuristic below; an explicit
+// split_k other than the row's keeps the heuristic's pipeline.
 const TableRow kTable[] = {
-    {FG_FP8_TENSOR, 1, 2048, 7168, 8, 2, 3},     {FG_FP8_TENSOR, 16, 2048, 7168, 8, 2, 3},
-    {FG_FP8_TENSOR, 1, 16384, 7168, 2, 2, 3},    {FG_FP8_TENSOR, 16, 16384, 7168, 2, 2, 3},
+    {FG_FP8_TENSOR, 1, 2048, 7168, 8, 1, 6},     {FG_FP8_TENSOR, 16, 2048, 7168, 8, 1, 6},
+    {FG_FP8_TENSOR, 1, 16384, 7168, 2, 2, 3},    {FG_FP8_TENSOR, 16, 16384, 7168, 1, 2, 5},
     {FG_FP8_BLOCK128, 1, 2048, 7168, 8, 1, 4},   {FG_FP8_BLOCK128, 16, 2048, 7168, 8, 1, 4},
     {FG_FP8_BLOCK128, 1, 16384, 7168, 2, 1, 4},  {FG_FP8_BLOCK128, 16, 16384, 7168, 2, 1, 4},
-    {FG_MXFP8, 1, 2048, 7168, 8, 1, 4},          {FG_MXFP8, 16, 2048, 7168, 8, 1, 4},
+    {FG_MXFP8, 1, 2048, 7168, 8, 1, 5},          {FG_MXFP8, 16, 2048, 7168, 8, 1, 4},
     {FG_MXFP8, 1, 16384, 7168, 2, 1, 4},         {FG_MXFP8, 16, 16384, 7168, 2, 1, 4},
-    {FG_MXFP4, 1, 2048, 7168, 4, 4, 2},          {FG_MXFP4, 16, 2048, 7168, 4, 4, 2},
+    {FG_MXFP4, 1, 2048, 7168, 8, 1, 4},          {FG_MXFP4, 16, 2048, 7168, 8, 1, 4},
     {FG_MXFP4, 1, 16384, 7168, 2, 1, 4},         {FG_MXFP4, 16, 16384, 7168, 2, 1, 4},
+    {FG_MXFP8_B32, 1, 2048, 7168, 8, 1, 5},      {FG_MXFP8_B32, 16, 2048, 7168, 8, 1, 4},
+    {FG_MXFP8_B32, 1, 16384, 7168, 2, 1, 4},     {FG_MXFP8_B32, 16, 16384, 7168, 2, 1, 4},
+    {FG_BF16, 1, 2048, 7168, 8, 1, 6},           {FG_BF16, 16, 2048, 7168, 8, 1, 6},
+    {FG_BF16, 1, 16384, 7168, 2, 2, 3},          {FG_BF16, 16, 16384, 7168, 2, 2, 3},
 };
 
 int64_t decode_row_limit() { return 32; }
@@ -181,8 +187,9 @@ fg_status make_plan(int mode, int64_t M, int64_t N, int64_t K, int split_k, fg_p
   int split = split_k, sps = 1, stages = 4;
   bool from_table = false;
   for (const TableRow& r : kTable) {
-    if (r.mode == mode && r.N == N && r.K == K && M <= r.m_max && (r.m_max == 1 ? M == 1 : M > 1)) {
-      if (split == 0) split = r.split;
+    if (r.mode == mode && r.N == N && r.K == K && M <= r.m_max && (r.m_max == 1 ? M == 1 : M > 1) &&
+        (split == 0 || split == r.split)) {
+      split = r.split;
       sps = r.sps;
       stages = r.stages;
       from_table = true;

@@ -382,8 +382,21 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int m = 0; m < kTokRows; ++m) comp[m] = 0.f;
       const float* a_s = static_cast<const float*>(p.a_scales);
       const int KS = p.K / 128;
+#pragma unroll 1
       for (int i = 0; i < nslab; ++i) {
         const int pb = i % C::NBUF;
+        // the slab's scales are loaded before the wait for its MMA, so their
+        // latency hides behind it
+        const int kb = u0 + i;
+        float w_s[kTokRows];
+        if (MODE == kBlock) {
+          const float bsc = __ldg(p.b_s + static_cast<size_t>(nt) * KS + kb);
+#pragma unroll
+          for (int m = 0; m < kTokRows; ++m) {
+            const int row = mt * kTokRows + m;
+            w_s[m] = (row < p.M ? __ldg(a_s + static_cast<size_t>(row) * KS + kb) : 0.f) * bsc;
+          }
+        }
         const bool w = mbar_wait(&pfull_bar[pb], (i / C::NBUF) & 1, T, p.err, 5);
         if (!__all_sync(0xffffffffu, w)) {
           ok = false;
@@ -396,14 +409,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&pempty_bar[pb]);
-        const int kb = u0 + i;
-        float bsc = 1.f;
-        if (MODE == kBlock) bsc = __ldg(p.b_s + static_cast<size_t>(nt) * KS + kb);
 #pragma unroll
         for (int m = 0; m < kTokRows; ++m) {
-          const int row = mt * kTokRows + m;
           float term = __uint_as_float(v[m]);
-          if (MODE == kBlock) term *= (row < p.M ? __ldg(a_s + static_cast<size_t>(row) * KS + kb) : 0.f) * bsc;
+          if (MODE == kBlock) term *= w_s[m];
           const float yk = term - comp[m];
           const float t = acc[m] + yk;
           comp[m] = (t - acc[m]) - yk;
@@ -541,6 +550,8 @@ cudaError_t launch_one(const CUtensorMap& tmap_a, const DecodeParams& p, dim3 gr
 // Instantiated configurations: (slabs per stage, stages).
 #define FG_DECODE_CONFIGS(X, MODE) \
   X(MODE, 1, 4)                    \
+  X(MODE, 1, 5)                    \
+  X(MODE, 1, 6)                    \
   X(MODE, 1, 8)                    \
   X(MODE, 2, 3)                    \
   X(MODE, 2, 5)                    \
@@ -550,8 +561,8 @@ cudaError_t launch_one(const CUtensorMap& tmap_a, const DecodeParams& p, dim3 gr
 
 bool decode_config_supported(const DecodeConfig& c) {
   if (c.mode < kBF16 || c.mode > kMXFP8B32) return false;
-  return (c.sps == 1 && (c.stages == 4 || c.stages == 8)) || (c.sps == 2 && (c.stages == 3 || c.stages == 5)) ||
-         (c.sps == 4 && c.stages == 2);
+  return (c.sps == 1 && (c.stages == 4 || c.stages == 5 || c.stages == 6 || c.stages == 8)) ||
+         (c.sps == 2 && (c.stages == 3 || c.stages == 5)) || (c.sps == 4 && c.stages == 2);
 }
 
 cudaError_t launch_decode(const DecodeConfig& c, const CUtensorMap& tmap_a, const DecodeParams& p, dim3 grid,

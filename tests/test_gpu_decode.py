@@ -84,6 +84,27 @@ def test_fused_uneven_split_matches_oracle(mode, S, M):
     assert fg.get_error() == fg.FG_OK
 
 
+PIPELINES = ["1,4", "1,5", "1,6", "1,8", "2,3", "2,5", "4,2"]
+
+
+@pytest.mark.parametrize("mode", MODES)
+@pytest.mark.parametrize("cfg", PIPELINES)
+def test_every_pipeline_config(mode, cfg, monkeypatch):
+    """Each instantiated (slabs per stage, stages) pipeline, forced through the
+    FG_DECODE_CONFIG hook: ragged token tile, splits 1 and 3 (three CTAs with
+    unequal K shares and unequal row counts), stage buffers reused several
+    times, every output against the oracle."""
+    monkeypatch.setenv("FG_DECODE_CONFIG", cfg)
+    M, N, K = 5, 256, 3072
+    c = Case(mode, *inputs.operands(mode, M, N, K, 700, 701, 702))
+    ref = c.ref()
+    for S in (1, 3):
+        plan = fg.gemm_plan(mode, M, N, K, split_k=S)
+        assert f"{plan['stage_slabs']},{plan['stages']}" == cfg
+        parity.assert_y_close(y_to_f64(c.gemm(split_k=S)), ref, f"{mode} {cfg} S={S}")
+    assert fg.get_error() == fg.FG_OK
+
+
 ONE = {"bf16": 0x3F80, "fp8_tensor": 0x38, "fp8_block128": 0x38, "mxfp8": 0x38, "mxfp4": 0x2,
        "mxfp8_b32": 0x38}
 
