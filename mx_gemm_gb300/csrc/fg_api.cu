@@ -162,6 +162,21 @@ int64_t decode_row_limit() { return 32; }
 // cluster size); larger splits take the two-pass workspace + reduce path.
 constexpr int kMaxClusterSplit = 8;
 
+// Output tile height of the large-M kernel: 256 x 256 tiles (both 128-row
+// halves of A against the same weight slabs in shared memory) for bf16 and
+// fp8 per-tensor once there are enough of them to fill the GPU's CTAs;
+// 128 x 256 (with the stream-K tail) otherwise and for MX.
+// FG_LARGE_TILE=128|256 overrides the choice for bf16 / fp8 (sweep hook).
+int large_tile_m(int mode, int64_t M, int64_t N) {
+  if (mode != FG_BF16 && mode != FG_FP8_TENSOR) return 128;
+  if (const char* ov = getenv("FG_LARGE_TILE")) {
+    if (strcmp(ov, "128") == 0) return 128;
+    if (strcmp(ov, "256") == 0) return 256;
+  }
+  const int64_t wide_tiles = ((M + 255) / 256) * (N / 256 + (N % 256 ? 1 : 0));
+  return wide_tiles >= sm_count() ? 256 : 128;
+}
+
 fg_status make_plan(int mode, int64_t M, int64_t N, int64_t K, int split_k, fg_plan* out) {
   memset(out, 0, sizeof *out);
   const int64_t Kb = row_bytes(mode, K);
@@ -174,14 +189,14 @@ fg_status make_plan(int mode, int64_t M, int64_t N, int64_t K, int split_k, fg_p
   if (large) {
     out->path = 1;
     out->split_k = 1;
-    out->tile_m = 128;
+    out->tile_m = large_tile_m(mode, M, N);
     out->tile_n = 256;
     out->stage_slabs = 1;
-    out->stages = 4;
-    const int64_t tiles = ((M + 127) / 128) * (N / 256 + (N % 256 ? 1 : 0));
+    out->stages = out->tile_m == 256 ? 3 : 4;
+    const int64_t tiles = ((M + out->tile_m - 1) / out->tile_m) * (N / 256 + (N % 256 ? 1 : 0));
     out->ctas = static_cast<int32_t>(tiles < sm_count() ? tiles : sm_count());
-    snprintf(out->name, sizeof out->name, "fg_large_sm103a_%s_m%lld_n%lld_k%lld_128x256", mode_name(mode),
-             (long long)M, (long long)N, (long long)K);
+    snprintf(out->name, sizeof out->name, "fg_large_sm103a_%s_m%lld_n%lld_k%lld_%dx256", mode_name(mode),
+             (long long)M, (long long)N, (long long)K, out->tile_m);
     return FG_OK;
   }
   int split = split_k, sps = 1, stages = 4;
@@ -447,8 +462,9 @@ fg_status fg_gemm_workspace_size(int mode, int64_t M, int64_t N, int64_t K, int 
   if (s != FG_OK) return s;
   if (plan.path == 1) {
     const int64_t tiles = ((M + 127) / 128) * (N / 256 + (N % 256 ? 1 : 0));
-    *bytes = is_mx(mode) ? sf_rows_image_bytes(mode, M, K)
-                         : large_streamk_plan(mode, tiles, row_bytes(mode, K) / 128, plan.ctas, nullptr);
+    *bytes = is_mx(mode)           ? sf_rows_image_bytes(mode, M, K)
+             : plan.tile_m == 256 ? 0
+                                  : large_streamk_plan(mode, tiles, row_bytes(mode, K) / 128, plan.ctas, nullptr);
   }
   else
     *bytes = plan.split_k > kMaxClusterSplit ? static_cast<uint64_t>(plan.split_k) * M * N * 4 : 0;
@@ -518,10 +534,13 @@ fg_status fg_gemm(const void* A, const void* a_scales, int64_t M, const fg_bshuf
     p.N = static_cast<int>(N);
     p.K = static_cast<int>(K);
     p.KB = static_cast<int>(rb / 128);
-    p.tiles_m = static_cast<int>((M + 127) / 128);
+    p.tiles_m = static_cast<int>((M + plan.tile_m - 1) / plan.tile_m);
     p.tiles_n = static_cast<int>(N / 256 + (N % 256 ? 1 : 0));
     p.debug_stall = (flags & FG_FLAG_DEBUG_STALL) ? 1 : 0;
-    if (!mx) {
+    p.wide = plan.tile_m == 256 ? 1 : 0;
+    if (p.wide) {
+      large_streamk_plan(mode, 0, 0, 0, &p);  // all tiles whole
+    } else if (!mx) {
       // the stream-K tail is an optimisation: only with a large enough workspace
       const uint64_t need = large_streamk_plan(mode, static_cast<int64_t>(p.tiles_m) * p.tiles_n, p.KB, plan.ctas, &p);
       if (need && workspace && workspace_bytes >= need && aligned(workspace, 16)) {

@@ -300,7 +300,11 @@ __global__ void __launch_bounds__(kThreads, 1)
           ++it;  // this stage's fill was consumed
           break;
         }
-        tc_commit(&empty_bar[slot]);
+        // Release the stage only if something waits for that: a refill
+        // (iteration it + STAGES) or, for the last such stage, the split-K
+        // receive area.  A commit stalls the MMA pipe for about as long as
+        // five of these MMAs, and the final commit covers the rest.
+        if (it + STAGES <= niter) tc_commit(&empty_bar[slot]);
       }
       consumed_sh = it;
       if (ok && !C::PROMOTE) tc_commit(&acc_bar);

@@ -330,6 +330,223 @@ cudaError_t launch_mode(const CUtensorMap& tmap_a, const LargeParams& p, int cta
 }
 
 
+// ---------------------------------------------------------- 256 x 256 form
+//
+// bf16 / fp8 per-tensor with 256 x 256 output tiles: per 128-byte K slab the
+// stage holds both 128-row halves of A (two TMA boxes) and both weight slabs,
+// and the MMA thread issues the four MMAs of each half against the same
+// weight slabs in shared memory.  Per 128 x 256 of output a stage then moves
+// 80 KiB through shared memory (TMA writes + MMA operand reads) instead of the
+// 96 KiB of the 128 x 256 tile -- the port that bounds the 128 x 256 kernel.
+// The two halves' accumulators fill TMEM (2 x 256 columns), so there is no
+// second accumulator to overlap the epilogue with: eight epilogue warps pull
+// half 0 into registers and release it (the next tile's half-0 MMAs may
+// start), store it, then do the same for half 1.  No stream-K tail.
+constexpr int kWideThreads = 320;
+constexpr int kWideBM = 256;
+constexpr int kWideStages = 3;
+constexpr int kWideABytes = kWideBM * 128;  // 32 KiB
+constexpr int kWideStageBytes = kWideABytes + kBBytes;
+constexpr int kWideSmem = kWideStages * kWideStageBytes + 1024;
+static_assert(kWideSmem <= 232448, "shared memory budget");
+
+template <int MODE>
+__global__ void __launch_bounds__(kWideThreads, 1)
+    large_wide_kernel(const __grid_constant__ CUtensorMap tmap_a, const LargeParams p) {
+  extern __shared__ uint8_t dsmem[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(dsmem) + 1023) & ~uintptr_t(1023));
+  __shared__ __align__(8) uint64_t full_bar[kWideStages];
+  __shared__ __align__(8) uint64_t empty_bar[kWideStages];
+  __shared__ __align__(8) uint64_t acce_bar[2];
+  __shared__ __align__(8) uint64_t accf_bar, stall_bar, drain_bar;
+  __shared__ uint32_t tmem_base_sh;
+  __shared__ int abort_sh, issued_sh, consumed_sh, mma_any_sh;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int tiles = p.tiles_m * p.tiles_n;
+  const int KB = p.KB;
+  const uint64_t T = p.timeout_ns;
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < kWideStages; ++i) {
+      mbar_init(&full_bar[i], 1);
+      mbar_init(&empty_bar[i], 1);
+    }
+    mbar_init(&acce_bar[0], 8);
+    mbar_init(&acce_bar[1], 8);
+    mbar_init(&accf_bar, 1);
+    mbar_init(&stall_bar, 1);
+    mbar_init(&drain_bar, 1);
+    abort_sh = 0;
+    issued_sh = 0;
+    consumed_sh = 0;
+    mma_any_sh = 0;
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(&tmem_base_sh, kTmemCols);
+    tmem_relinquish();
+  }
+  if (warp == 0 && lane == 0) prefetch_tmap(&tmap_a);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = tmem_base_sh;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      int it = 0;
+      bool ok = true;
+      for (int t = blockIdx.x; ok && t < tiles; t += gridDim.x) {
+        const TileCoord tc = tile_coord(t, p.tiles_m, p.tiles_n);
+        const int nslabs_n = min(2, p.N / 128 - 2 * tc.n);
+        for (int kb = 0; kb < KB; ++kb, ++it) {
+          const int slot = it % kWideStages;
+          if (!mbar_wait(&empty_bar[slot], ((it / kWideStages) & 1) ^ 1u, T, p.err, 31)) {
+            ok = false;
+            break;
+          }
+          uint8_t* st = smem + slot * kWideStageBytes;
+          mbar_arrive_expect_tx(&full_bar[slot], kWideABytes + nslabs_n * 16384);
+          tma_load_2d(st, &tmap_a, kb * 128, tc.m * kWideBM, &full_bar[slot]);
+          tma_load_2d(st + kABytes, &tmap_a, kb * 128, tc.m * kWideBM + kBM, &full_bar[slot]);
+          for (int h = 0; h < nslabs_n; ++h)
+            bulk_g2s(st + kWideABytes + h * 16384,
+                     p.b_img + (static_cast<size_t>(2 * tc.n + h) * KB + kb) * 16384, 16384, &full_bar[slot]);
+        }
+      }
+      issued_sh = it;
+      if (!ok) abort_sh = 1;
+    }
+  } else if (warp == 1) {
+    // ---------------------------------------------------------- MMA issuer
+    if (lane == 0) {
+      bool ok = true;
+      if (p.debug_stall) ok = mbar_wait(&stall_bar, 0, T, p.err, 32);
+      int it = 0, ti = 0;
+      const uint32_t idesc = MODE == kBF16 ? idesc_bf16(kBM, kBN) : idesc_e4m3(kBM, kBN);
+      for (int t = blockIdx.x; ok && t < tiles; t += gridDim.x, ++ti) {
+        for (int kb = 0; kb < KB; ++kb, ++it) {
+          const int slot = it % kWideStages;
+          if (!mbar_wait(&full_bar[slot], (it / kWideStages) & 1, T, p.err, 33)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          mma_any_sh = 1;
+          uint8_t* st = smem + slot * kWideStageBytes;
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            if (kb == 0) {
+              // half h of the accumulator: drained by the epilogue of the previous tile
+              if (!mbar_wait(&acce_bar[h], (ti & 1) ^ 1u, T, p.err, 34)) {
+                ok = false;
+                break;
+              }
+              tc_fence_after();
+            }
+            const uint32_t d = tmem + h * kBN;
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+              const uint64_t adesc = sdesc_sw128(smem_u32(st + h * kABytes + j * 32));
+              const uint64_t bdesc = sdesc_sw128(smem_u32(st + kWideABytes + j * 32));
+              const uint32_t accum = (kb > 0 || j > 0) ? 1u : 0u;
+              if (MODE == kBF16)
+                mma_f16(d, adesc, bdesc, idesc, accum);
+              else
+                mma_f8f6f4(d, adesc, bdesc, idesc, accum);
+            }
+          }
+          if (!ok) {
+            ++it;  // this stage's fill was consumed
+            break;
+          }
+          tc_commit(&empty_bar[slot]);
+        }
+        if (!ok) break;
+        tc_commit(&accf_bar);
+      }
+      consumed_sh = it;
+      if (!ok) abort_sh = 1;
+      if (mma_any_sh) {
+        tc_commit(&drain_bar);
+        mbar_wait(&drain_bar, 0, T, p.err, 35);
+      }
+    }
+  } else {
+    // -------------------------------------------- epilogue (eight warps)
+    // lane quarter warp % 4 (the TMEM lanes this warp may read), column half
+    // (warp - 2) / 4 of each accumulator half
+    const int qd = warp & 3;
+    const int chalf = (warp - 2) >> 2;
+    float scale = 1.f;
+    if (MODE == kTensor) scale = __ldg(static_cast<const float*>(p.a_scales)) * __ldg(p.b_s);
+    int ti = 0;
+    for (int t = blockIdx.x; t < tiles; t += gridDim.x, ++ti) {
+      const bool w = mbar_wait(&accf_bar, ti & 1, T, p.err, 36);
+      if (!__all_sync(0xffffffffu, w)) {
+        if (lane == 0) abort_sh = 1;
+        break;
+      }
+      tc_fence_after();
+      const TileCoord tc = tile_coord(t, p.tiles_m, p.tiles_n);
+      const int col0 = tc.n * kBN + chalf * 128;
+#pragma unroll 1
+      for (int h = 0; h < 2; ++h) {
+        uint32_t v[128];
+        const uint32_t taddr = tmem + h * kBN + chalf * 128 + (static_cast<uint32_t>(qd * 32) << 16);
+        tmem_ld32(taddr + 0, *reinterpret_cast<uint32_t(*)[32]>(&v[0]));
+        tmem_ld32(taddr + 32, *reinterpret_cast<uint32_t(*)[32]>(&v[32]));
+        tmem_ld32(taddr + 64, *reinterpret_cast<uint32_t(*)[32]>(&v[64]));
+        tmem_ld32(taddr + 96, *reinterpret_cast<uint32_t(*)[32]>(&v[96]));
+        tmem_wait_ld();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&acce_bar[h]);  // half h free: the next tile's MMAs may write it
+        const int row = tc.m * kWideBM + h * kBM + qd * 32 + lane;
+        if (row < p.M && col0 < p.N) {
+          uint4* dst = reinterpret_cast<uint4*>(p.y + static_cast<size_t>(row) * p.N + col0);
+#pragma unroll
+          for (int q = 0; q < 16; ++q) {
+            uint4 o;
+            o.x = pack_bf16x2(__uint_as_float(v[8 * q + 0]) * scale, __uint_as_float(v[8 * q + 1]) * scale);
+            o.y = pack_bf16x2(__uint_as_float(v[8 * q + 2]) * scale, __uint_as_float(v[8 * q + 3]) * scale);
+            o.z = pack_bf16x2(__uint_as_float(v[8 * q + 4]) * scale, __uint_as_float(v[8 * q + 5]) * scale);
+            o.w = pack_bf16x2(__uint_as_float(v[8 * q + 6]) * scale, __uint_as_float(v[8 * q + 7]) * scale);
+            dst[q] = o;
+          }
+        }
+      }
+    }
+  }
+
+  // ------------------------------------------------------------- teardown
+  tc_fence_before();
+  __syncthreads();
+  if (abort_sh && threadIdx.x == 0) {
+    for (int it = consumed_sh; it < issued_sh; ++it)
+      mbar_wait(&full_bar[it % kWideStages], (it / kWideStages) & 1, T, nullptr, 0);
+  }
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 1) tmem_dealloc(tmem, kTmemCols);
+}
+
+template <int MODE>
+cudaError_t launch_wide(const CUtensorMap& tmap_a, const LargeParams& p, int ctas, cudaStream_t stream) {
+  static bool attr_set = false;
+  if (!attr_set) {
+    cudaError_t e =
+        cudaFuncSetAttribute(large_wide_kernel<MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize, kWideSmem);
+    if (e != cudaSuccess) return e;
+    attr_set = true;
+  }
+  large_wide_kernel<MODE><<<ctas, kWideThreads, kWideSmem, stream>>>(tmap_a, p);
+  return cudaGetLastError();
+}
+
+
 // ------------------------------------------------------------------ MX form
 //
 // Block-scaled variant (mxfp8: kind::mxf8f6f4, one E8M0 per 32 K of the
@@ -558,6 +775,11 @@ uint64_t large_streamk_bytes(int ctas) {
 bool large_supported(int mode) { return mode == kBF16 || mode == kTensor || is_mx(mode); }
 
 cudaError_t launch_large(int mode, const CUtensorMap& tmap_a, const LargeParams& p, int ctas, cudaStream_t stream) {
+  if (p.wide) {
+    if (mode == kBF16) return launch_wide<kBF16>(tmap_a, p, ctas, stream);
+    if (mode == kTensor) return launch_wide<kTensor>(tmap_a, p, ctas, stream);
+    return cudaErrorNotSupported;
+  }
   if (mode == kBF16) return launch_mode<kBF16>(tmap_a, p, ctas, stream);
   if (mode == kTensor) return launch_mode<kTensor>(tmap_a, p, ctas, stream);
   if (mode == kMXFP8) return launch_mx<kMXFP8>(tmap_a, p, ctas, stream);

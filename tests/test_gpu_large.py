@@ -116,3 +116,53 @@ def test_large_bounded_wait_reports_timeout(mode, M, N, K, streamk):
     rows = inputs.sample_rows(M, n=64)
     y = c.gemm(workspace=ws)
     parity.assert_y_close(y_to_f64(y[torch.from_numpy(rows).cuda()]), c.ref(rows=rows), f"{mode} after timeout")
+
+
+@pytest.mark.parametrize("mode", ["bf16", "fp8_tensor"])
+@pytest.mark.parametrize("M,N,K", [(257, 256, 512), (300, 384, 1024), (1000, 1280, 1536)])
+def test_wide_tile_small_shapes(mode, M, N, K, monkeypatch):
+    """The 256 x 256 form forced on small shapes: a second 128-row half that
+    is partly or wholly past M, a last weight tile with one slab; every
+    output against the oracle."""
+    monkeypatch.setenv("FG_LARGE_TILE", "256")
+    c = Case(mode, *inputs.operands(mode, M, N, K, 40 + M, 50 + N, 60 + K))
+    plan = fg.gemm_plan(mode, M, N, K)
+    assert plan["path"] == 1 and plan["tile_m"] == 256
+    assert fg.gemm_workspace_size(mode, M, N, K) == 0
+    parity.assert_y_close(y_to_f64(c.gemm()), c.ref(), f"{mode} {M}x{N}x{K} 256x256")
+    assert fg.get_error() == fg.FG_OK
+
+
+@pytest.mark.parametrize("mode", ["bf16", "fp8_tensor"])
+def test_wide_and_narrow_tiles_agree_bit_for_bit(mode, monkeypatch):
+    """Both large-M forms accumulate every output over the same K order with
+    the same MMA shape: without the stream-K tail their results are the same
+    bits.  160 wide tiles on the GPU's CTAs: some CTAs run two tiles, so the
+    accumulator hand-over between tiles is exercised."""
+    M, N, K = 2560, 4096, 1024
+    c = Case(mode, *inputs.operands(mode, M, N, K, 71, 72, 73))
+    no_ws = torch.empty(4, dtype=torch.float32, device="cuda")   # too small: no stream-K
+    monkeypatch.setenv("FG_LARGE_TILE", "256")
+    y_wide = c.gemm(workspace=no_ws)
+    monkeypatch.setenv("FG_LARGE_TILE", "128")
+    y_narrow = c.gemm(workspace=no_ws)
+    assert torch.equal(y_wide.view(torch.int16), y_narrow.view(torch.int16))
+    rows = inputs.sample_rows(M, n=64)
+    parity.assert_y_close(y_to_f64(y_wide[torch.from_numpy(rows).cuda()]), c.ref(rows=rows), f"{mode} wide")
+    assert fg.get_error() == fg.FG_OK
+
+
+@pytest.mark.parametrize("mode", ["bf16", "fp8_tensor"])
+def test_wide_tile_bounded_wait_reports_timeout(mode, monkeypatch):
+    monkeypatch.setenv("FG_LARGE_TILE", "256")
+    M, N, K = 600, 512, 1024
+    c = Case(mode, *inputs.operands(mode, M, N, K, 84, 85, 86))
+    assert fg.get_error() == fg.FG_OK
+    fg.set_wait_timeout_ns(20_000_000)
+    try:
+        c.gemm(flags=fg.FG_FLAG_DEBUG_STALL)
+        assert fg.get_error() == fg.FG_ERR_TIMEOUT
+    finally:
+        fg.set_wait_timeout_ns(4_000_000_000)
+    assert fg.get_error() == fg.FG_OK
+    parity.assert_y_close(y_to_f64(c.gemm()), c.ref(), f"{mode} 256x256 after timeout")
