@@ -250,7 +250,7 @@ fg_status make_plan(int mode, int64_t M, int64_t N, int64_t K, int split_k, fg_p
 // Stream-K tail of the large-M bf16 / fp8 kernel: used when the tile count
 // leaves a partial last wave.  Fills the schedule fields of p; returns the
 // workspace bytes it needs (0 = every tile is processed whole).
-uint64_t large_streamk_plan(int mode, int64_t tiles, int64_t KB, int ctas, LargeParams* p) {
+uint64_t large_streamk_plan(int mode, int64_t tiles, int64_t KB, int ctas, LargeParams* p, bool wide) {
   if (p) {
     p->dp_rounds = 0;
     p->dp_tiles = 0;
@@ -258,6 +258,9 @@ uint64_t large_streamk_plan(int mode, int64_t tiles, int64_t KB, int ctas, Large
   }
   if (is_mx(mode) || ctas <= 0 || tiles <= ctas || tiles % ctas == 0) return 0;
   const int64_t full_waves = tiles / ctas;
+  // 256 x 256 tiles: measured slower (by ~20 us) when every tile is split,
+  // i.e. with fewer than two full waves; there the whole-tile schedule is kept
+  if (wide && full_waves < 2) return 0;
   const int64_t dp_rounds = full_waves - 1;
   const int64_t sk_tiles = tiles - dp_rounds * ctas;  // >= ctas: every CTA range spans >= one tile of K
   if (p) {
@@ -265,7 +268,7 @@ uint64_t large_streamk_plan(int mode, int64_t tiles, int64_t KB, int ctas, Large
     p->dp_tiles = static_cast<int>(dp_rounds * ctas);
     p->sk_iters = sk_tiles * KB;
   }
-  return large_streamk_bytes(ctas);
+  return large_streamk_bytes(ctas, wide);
 }
 
 // A 64-bit tag per launch: a stream-K flag matches only the launch that
@@ -461,10 +464,10 @@ fg_status fg_gemm_workspace_size(int mode, int64_t M, int64_t N, int64_t K, int 
   fg_status s = fg_gemm_plan(mode, M, N, K, split_k, &plan);
   if (s != FG_OK) return s;
   if (plan.path == 1) {
-    const int64_t tiles = ((M + 127) / 128) * (N / 256 + (N % 256 ? 1 : 0));
-    *bytes = is_mx(mode)           ? sf_rows_image_bytes(mode, M, K)
-             : plan.tile_m == 256 ? 0
-                                  : large_streamk_plan(mode, tiles, row_bytes(mode, K) / 128, plan.ctas, nullptr);
+    const int64_t tiles = ((M + plan.tile_m - 1) / plan.tile_m) * (N / 256 + (N % 256 ? 1 : 0));
+    *bytes = is_mx(mode) ? sf_rows_image_bytes(mode, M, K)
+                         : large_streamk_plan(mode, tiles, row_bytes(mode, K) / 128, plan.ctas, nullptr,
+                                              plan.tile_m == 256);
   }
   else
     *bytes = plan.split_k > kMaxClusterSplit ? static_cast<uint64_t>(plan.split_k) * M * N * 4 : 0;
@@ -538,18 +541,17 @@ fg_status fg_gemm(const void* A, const void* a_scales, int64_t M, const fg_bshuf
     p.tiles_n = static_cast<int>(N / 256 + (N % 256 ? 1 : 0));
     p.debug_stall = (flags & FG_FLAG_DEBUG_STALL) ? 1 : 0;
     p.wide = plan.tile_m == 256 ? 1 : 0;
-    if (p.wide) {
-      large_streamk_plan(mode, 0, 0, 0, &p);  // all tiles whole
-    } else if (!mx) {
+    if (!mx) {
       // the stream-K tail is an optimisation: only with a large enough workspace
-      const uint64_t need = large_streamk_plan(mode, static_cast<int64_t>(p.tiles_m) * p.tiles_n, p.KB, plan.ctas, &p);
+      const uint64_t need =
+          large_streamk_plan(mode, static_cast<int64_t>(p.tiles_m) * p.tiles_n, p.KB, plan.ctas, &p, p.wide != 0);
       if (need && workspace && workspace_bytes >= need && aligned(workspace, 16)) {
         p.sk_part = static_cast<float*>(workspace);
-        p.sk_flag = reinterpret_cast<unsigned long long*>(static_cast<uint8_t*>(workspace) +
-                                                           need - static_cast<uint64_t>(plan.ctas) * 32);
+        p.sk_flag = reinterpret_cast<unsigned long long*>(static_cast<uint8_t*>(workspace) + need -
+                                                           static_cast<uint64_t>(plan.ctas) * (p.wide ? 64 : 32));
         p.epoch = next_epoch();
       } else {
-        large_streamk_plan(mode, 0, 0, 0, &p);  // all tiles whole
+        large_streamk_plan(mode, 0, 0, 0, &p, false);  // all tiles whole
       }
     }
     if (mx) {

@@ -66,13 +66,14 @@ struct LargeParams {
   int dp_rounds;
   int dp_tiles;
   long long sk_iters;
-  float* sk_part;                  // [G][256 columns][128 rows] fp32
-  unsigned long long* sk_flag;     // [G][4 warps]: equals `epoch` once published
+  float* sk_part;                  // [G][256 columns][128 rows] fp32 ([G][2 halves][256][128] when wide)
+  unsigned long long* sk_flag;     // [G][4 warps] ([G][8 warps] when wide): equals `epoch` once published
   unsigned long long epoch;
 };
 
-// Bytes of the optional stream-K workspace of the large-M bf16 / fp8 kernel.
-uint64_t large_streamk_bytes(int ctas);
+// Bytes of the optional stream-K workspace of the large-M bf16 / fp8 kernel
+// (128 x 256 or, wide, 256 x 256 tiles).
+uint64_t large_streamk_bytes(int ctas, bool wide);
 
 bool decode_config_supported(const DecodeConfig& c);
 // Kernels are launched with programmatic dependent launch (they may start

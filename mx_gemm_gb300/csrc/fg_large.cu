@@ -341,7 +341,11 @@ cudaError_t launch_mode(const CUtensorMap& tmap_a, const LargeParams& p, int cta
 // The two halves' accumulators fill TMEM (2 x 256 columns), so there is no
 // second accumulator to overlap the epilogue with: eight epilogue warps pull
 // half 0 into registers and release it (the next tile's half-0 MMAs may
-// start), store it, then do the same for half 1.  No stream-K tail.
+// start), store it, then do the same for half 1.
+//
+// Stream-K tail as in the 128 x 256 form (same chunk walk): a CTA holding a
+// tile's last K iterations publishes both halves' fp32 partials, one flag
+// per epilogue warp; the CTA holding the tile's first iterations adds them.
 constexpr int kWideThreads = 320;
 constexpr int kWideBM = 256;
 constexpr int kWideStages = 3;
@@ -398,10 +402,12 @@ __global__ void __launch_bounds__(kWideThreads, 1)
     if (lane == 0) {
       int it = 0;
       bool ok = true;
-      for (int t = blockIdx.x; ok && t < tiles; t += gridDim.x) {
-        const TileCoord tc = tile_coord(t, p.tiles_m, p.tiles_n);
+      const int nch = chunk_count(p, blockIdx.x, gridDim.x, tiles, KB);
+      for (int ci = 0; ok && ci < nch; ++ci) {
+        const Chunk ch = chunk_at(p, blockIdx.x, gridDim.x, KB, ci);
+        const TileCoord tc = tile_coord(ch.t, p.tiles_m, p.tiles_n);
         const int nslabs_n = min(2, p.N / 128 - 2 * tc.n);
-        for (int kb = 0; kb < KB; ++kb, ++it) {
+        for (int kb = ch.k0; kb < ch.k1; ++kb, ++it) {
           const int slot = it % kWideStages;
           if (!mbar_wait(&empty_bar[slot], ((it / kWideStages) & 1) ^ 1u, T, p.err, 31)) {
             ok = false;
@@ -424,10 +430,12 @@ __global__ void __launch_bounds__(kWideThreads, 1)
     if (lane == 0) {
       bool ok = true;
       if (p.debug_stall) ok = mbar_wait(&stall_bar, 0, T, p.err, 32);
-      int it = 0, ti = 0;
+      int it = 0;
       const uint32_t idesc = MODE == kBF16 ? idesc_bf16(kBM, kBN) : idesc_e4m3(kBM, kBN);
-      for (int t = blockIdx.x; ok && t < tiles; t += gridDim.x, ++ti) {
-        for (int kb = 0; kb < KB; ++kb, ++it) {
+      const int nch = chunk_count(p, blockIdx.x, gridDim.x, tiles, KB);
+      for (int ti = 0; ok && ti < nch; ++ti) {
+        const Chunk ch = chunk_at(p, blockIdx.x, gridDim.x, KB, ti);
+        for (int kb = ch.k0; kb < ch.k1; ++kb, ++it) {
           const int slot = it % kWideStages;
           if (!mbar_wait(&full_bar[slot], (it / kWideStages) & 1, T, p.err, 33)) {
             ok = false;
@@ -438,8 +446,8 @@ __global__ void __launch_bounds__(kWideThreads, 1)
           uint8_t* st = smem + slot * kWideStageBytes;
 #pragma unroll
           for (int h = 0; h < 2; ++h) {
-            if (kb == 0) {
-              // half h of the accumulator: drained by the epilogue of the previous tile
+            if (kb == ch.k0) {
+              // half h of the accumulator: drained by the epilogue of the previous chunk
               if (!mbar_wait(&acce_bar[h], (ti & 1) ^ 1u, T, p.err, 34)) {
                 ok = false;
                 break;
@@ -451,7 +459,7 @@ __global__ void __launch_bounds__(kWideThreads, 1)
             for (int j = 0; j < 4; ++j) {
               const uint64_t adesc = sdesc_sw128(smem_u32(st + h * kABytes + j * 32));
               const uint64_t bdesc = sdesc_sw128(smem_u32(st + kWideABytes + j * 32));
-              const uint32_t accum = (kb > 0 || j > 0) ? 1u : 0u;
+              const uint32_t accum = (kb > ch.k0 || j > 0) ? 1u : 0u;
               if (MODE == kBF16)
                 mma_f16(d, adesc, bdesc, idesc, accum);
               else
@@ -482,16 +490,30 @@ __global__ void __launch_bounds__(kWideThreads, 1)
     const int chalf = (warp - 2) >> 2;
     float scale = 1.f;
     if (MODE == kTensor) scale = __ldg(static_cast<const float*>(p.a_scales)) * __ldg(p.b_s);
-    int ti = 0;
-    for (int t = blockIdx.x; t < tiles; t += gridDim.x, ++ti) {
+    const int ew = warp - 2;  // epilogue warp 0..7: its stream-K flag
+    const int nch = chunk_count(p, blockIdx.x, gridDim.x, tiles, KB);
+    for (int ti = 0; ti < nch; ++ti) {
+      const Chunk ch = chunk_at(p, blockIdx.x, gridDim.x, KB, ti);
       const bool w = mbar_wait(&accf_bar, ti & 1, T, p.err, 36);
       if (!__all_sync(0xffffffffu, w)) {
         if (lane == 0) abort_sh = 1;
         break;
       }
       tc_fence_after();
-      const TileCoord tc = tile_coord(t, p.tiles_m, p.tiles_n);
+      const TileCoord tc = tile_coord(ch.t, p.tiles_m, p.tiles_n);
       const int col0 = tc.n * kBN + chalf * 128;
+      const int lrow = qd * 32 + lane;
+      // stream-K partials: [CTA][half][256 columns][128 rows] fp32
+      const bool publish = ch.k0 > 0;   // this CTA holds the tile's last iterations
+      const bool finish = !publish && ch.k1 < KB;  // the rest comes from CTA blockIdx.x + 1
+      bool have_peer = true;
+      if (finish) {
+        bool fw = true;
+        if (lane == 0) fw = wait_flag_eq(p.sk_flag + (blockIdx.x + 1) * 8 + ew, p.epoch, T, p.err, 37);
+        have_peer = __shfl_sync(0xffffffffu, fw ? 1 : 0, 0) != 0;
+        if (have_peer) (void)ld_acquire_u64(p.sk_flag + (blockIdx.x + 1) * 8 + ew);
+        else if (lane == 0) abort_sh = 1;
+      }
 #pragma unroll 1
       for (int h = 0; h < 2; ++h) {
         uint32_t v[128];
@@ -503,9 +525,21 @@ __global__ void __launch_bounds__(kWideThreads, 1)
         tmem_wait_ld();
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(&acce_bar[h]);  // half h free: the next tile's MMAs may write it
-        const int row = tc.m * kWideBM + h * kBM + qd * 32 + lane;
-        if (row < p.M && col0 < p.N) {
+        if (lane == 0) mbar_arrive(&acce_bar[h]);  // half h free: the next chunk's MMAs may write it
+        const size_t pbase = static_cast<size_t>(h) * kBN * kBM + static_cast<size_t>(chalf) * 128 * kBM + lrow;
+        if (publish) {
+          float* part = p.sk_part + static_cast<size_t>(blockIdx.x) * 2 * kBN * kBM + pbase;
+#pragma unroll
+          for (int i = 0; i < 128; ++i) __stcg(part + i * kBM, __uint_as_float(v[i]));
+          continue;
+        }
+        if (finish && have_peer) {
+          const float* peer = p.sk_part + static_cast<size_t>(blockIdx.x + 1) * 2 * kBN * kBM + pbase;
+#pragma unroll
+          for (int i = 0; i < 128; ++i) v[i] = __float_as_uint(__uint_as_float(v[i]) + __ldcg(peer + i * kBM));
+        }
+        const int row = tc.m * kWideBM + h * kBM + lrow;
+        if (row < p.M && col0 < p.N && have_peer) {
           uint4* dst = reinterpret_cast<uint4*>(p.y + static_cast<size_t>(row) * p.N + col0);
 #pragma unroll
           for (int q = 0; q < 16; ++q) {
@@ -517,6 +551,11 @@ __global__ void __launch_bounds__(kWideThreads, 1)
             dst[q] = o;
           }
         }
+      }
+      if (publish) {
+        __threadfence();
+        __syncwarp();
+        if (lane == 0) st_release_u64(p.sk_flag + blockIdx.x * 8 + ew, p.epoch);
       }
     }
   }
@@ -542,8 +581,17 @@ cudaError_t launch_wide(const CUtensorMap& tmap_a, const LargeParams& p, int cta
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
-  large_wide_kernel<MODE><<<ctas, kWideThreads, kWideSmem, stream>>>(tmap_a, p);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(ctas);
+  cfg.blockDim = dim3(kWideThreads);
+  cfg.dynamicSmemBytes = kWideSmem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr;
+  attr.id = cudaLaunchAttributeCooperative;  // stream-K CTAs wait on one another: all must be resident
+  attr.val.cooperative = 1;
+  cfg.attrs = &attr;
+  cfg.numAttrs = p.sk_iters > 0 ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, large_wide_kernel<MODE>, tmap_a, p);
 }
 
 
@@ -768,8 +816,9 @@ cudaError_t launch_mx(const CUtensorMap& tmap_a, const LargeParams& p, int ctas,
 
 }  // namespace
 
-uint64_t large_streamk_bytes(int ctas) {
-  return static_cast<uint64_t>(ctas) * (static_cast<uint64_t>(kBN) * kBM * 4 + 4 * 8);
+uint64_t large_streamk_bytes(int ctas, bool wide) {
+  return wide ? static_cast<uint64_t>(ctas) * (2ull * kBN * kBM * 4 + 8 * 8)
+              : static_cast<uint64_t>(ctas) * (static_cast<uint64_t>(kBN) * kBM * 4 + 4 * 8);
 }
 
 bool large_supported(int mode) { return mode == kBF16 || mode == kTensor || is_mx(mode); }

@@ -69,11 +69,14 @@ def test_large_workload_parity_sampled_rows(mode, M, N, K, name, idx):
 
 
 @pytest.mark.parametrize("mode", ["bf16", "fp8_tensor"])
-def test_streamk_tail_matches_whole_tiles(mode):
-    """160 tiles on the GPU's CTAs leave a partial wave: with the workspace
-    the tail runs stream-K (tiles split between CTAs, fp32 partials passed
-    between them); without it every tile runs whole.  Both match the oracle."""
-    M, N, K = 2560, 2048, 2048
+@pytest.mark.parametrize("tile,M,N,K", [("128", 2560, 2048, 2048), ("256", 6144, 6144, 1024)])
+def test_streamk_tail_matches_whole_tiles(mode, tile, M, N, K, monkeypatch):
+    """160 (128 x 256) or 576 (256 x 256) tiles on the GPU's CTAs leave a
+    partial wave: with the workspace the tail runs stream-K (tiles split
+    between CTAs, fp32 partials passed between them); without it every tile
+    runs whole.  Both match the oracle."""
+    monkeypatch.setenv("FG_LARGE_TILE", tile)
+    assert fg.gemm_plan(mode, M, N, K)["tile_m"] == int(tile)
     c = Case(mode, *inputs.operands(mode, M, N, K, 91, 92, 93))
     need = fg.gemm_workspace_size(mode, M, N, K)
     assert need > 0
