@@ -24,7 +24,7 @@ import math
 
 import numpy as np
 
-MODES = ("bf16", "fp8_tensor", "fp8_block128", "mxfp8", "mxfp4", "mxfp8_b32")
+MODES = ("bf16", "fp8_tensor", "fp8_block128", "mxfp8", "mxfp4", "mxfp8_b32", "mxfp4_fp8a")
 E4M3_MAX = 448.0
 E2M1_MAX = 6.0
 _E2M1_MAG = np.array([0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0], np.float64)
@@ -156,6 +156,10 @@ def operands(mode, M, N, K, seed_a, seed_b, seed_s):
         A, a_s = mx_operand(M, K, seed_a, mode)
         B, b_s = mx_operand(N, K, seed_b, mode)
         return A, B, a_s, b_s
+    if mode == "mxfp4_fp8a":   # fp8 activations (32-K E8M0), fp4 weights (32-K E8M0)
+        A, a_s = mx_operand(M, K, seed_a, "mxfp8_b32")
+        B, b_s = mx_operand(N, K, seed_b, "mxfp4")
+        return A, B, a_s, b_s
     raise ValueError(mode)
 
 
@@ -189,6 +193,9 @@ WORKLOADS = {
     "mx_mxfp8_mxfp4_n16384_k7168": dict(
         idx=4, cases=[dict(mode=f, M=m, N=16384, K=7168, split_k=0)
                       for f in ("mxfp8", "mxfp4") for m in (1, 16, 4096)]),
+    # next: fp8 activations against fp4 weights (the MX shapes above)
+    "mx_fp8a_fp4w_n16384_k7168": dict(
+        idx=5, cases=[dict(mode="mxfp4_fp8a", M=m, N=16384, K=7168, split_k=0) for m in (1, 16, 4096)]),
 }
 
 

@@ -19,9 +19,9 @@ import numpy as np
 
 from . import build as _build
 
-BF16, FP8_TENSOR, FP8_BLOCK128, MXFP8, MXFP4, MXFP8_B32 = 0, 1, 2, 3, 4, 5
+BF16, FP8_TENSOR, FP8_BLOCK128, MXFP8, MXFP4, MXFP8_B32, MXFP4_FP8A = 0, 1, 2, 3, 4, 5, 6
 MODE_NAMES = {BF16: "bf16", FP8_TENSOR: "fp8_tensor", FP8_BLOCK128: "fp8_block128",
-              MXFP8: "mxfp8", MXFP4: "mxfp4", MXFP8_B32: "mxfp8_b32"}
+              MXFP8: "mxfp8", MXFP4: "mxfp4", MXFP8_B32: "mxfp8_b32", MXFP4_FP8A: "mxfp4_fp8a"}
 
 _lib = None
 
@@ -42,6 +42,10 @@ def lib():
         L.orc_preshuffle_b.restype = ctypes.c_int
         L.orc_unshuffle_b.argtypes = [vp, i64, i64, vp]
         L.orc_unshuffle_b.restype = ctypes.c_int
+        L.orc_block64_b.argtypes = [vp, i64, i64, vp]
+        L.orc_block64_b.restype = ctypes.c_int
+        L.orc_unblock64_b.argtypes = [vp, i64, i64, vp]
+        L.orc_unblock64_b.restype = ctypes.c_int
         L.orc_sf_image.argtypes = [ctypes.c_int, vp, i64, i64, vp]
         L.orc_sf_image.restype = ctypes.c_int
         L.orc_round_bf16.argtypes = [vp, i64, vp]
@@ -102,7 +106,7 @@ def gemm(mode, A, B, a_scale=None, b_scale=None, M=None, N=None, K=None,
     uint8 e4m3 codes [M][K], or uint8 packed e2m1 pairs [M][K/2].  Scales:
     fp32 scalars (FP8_TENSOR), fp32 [M][K/128] and [N/128][K/128]
     (FP8_BLOCK128), uint8 E8M0 [M][K/128] (MXFP8) or [M][K/32] (MXFP4,
-    MXFP8_B32).
+    MXFP8_B32, MXFP4_FP8A).  MXFP4_FP8A: A e4m3 [M][K], B packed e2m1 [N][K/2].
     ``tensor_scale`` False gives the unscaled per-tensor sum, which is what a
     split-K partial holds in that mode.
     """
@@ -119,7 +123,7 @@ def gemm(mode, A, B, a_scale=None, b_scale=None, M=None, N=None, K=None,
     if mode in (FP8_TENSOR, FP8_BLOCK128):
         a_scale = _c(np.asarray(a_scale, np.float32).reshape(-1), np.float32)
         b_scale = _c(np.asarray(b_scale, np.float32).reshape(-1), np.float32)
-    elif mode in (MXFP8, MXFP4, MXFP8_B32):
+    elif mode in (MXFP8, MXFP4, MXFP8_B32, MXFP4_FP8A):
         a_scale, b_scale = _c(a_scale, np.uint8), _c(b_scale, np.uint8)
     else:
         a_scale = b_scale = None
@@ -166,6 +170,24 @@ def unshuffle_b(img, N, Kb):
     out = np.empty((N, Kb), np.uint8)
     if lib().orc_unshuffle_b(_ptr(img), N, Kb, _ptr(out)) != 0:
         raise ValueError("bad preshuffle shape")
+    return out
+
+
+def block64_b(B_bytes, N, Kb):
+    """MXFP4_FP8A weight image (layout spec): 128-row x 64-byte blocks of the
+    packed fp4 bytes, unswizzled."""
+    B_bytes = _c(B_bytes, np.uint8)
+    out = np.empty(N * Kb, np.uint8)
+    if lib().orc_block64_b(_ptr(B_bytes), N, Kb, _ptr(out)) != 0:
+        raise ValueError("bad block shape")
+    return out
+
+
+def unblock64_b(img, N, Kb):
+    img = _c(img, np.uint8)
+    out = np.empty((N, Kb), np.uint8)
+    if lib().orc_unblock64_b(_ptr(img), N, Kb, _ptr(out)) != 0:
+        raise ValueError("bad block shape")
     return out
 
 

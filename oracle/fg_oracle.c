@@ -25,7 +25,10 @@
  *                byte, low nibble = even k
  *   MXFP8_B32    Ad = e4m3(a) * 2^(a_sf[m][k/32]-127)      (the OCP MX block of
  *                32 elements, next to the pages' 128-element "mx128")
- * and the same for B with n in place of m.
+ * and the same for B with n in place of m, except
+ *   MXFP4_FP8A   Ad as MXFP8_B32, Bd as MXFP4: fp8 activations against fp4
+ *                weights, both with one E8M0 per 32 K (the FlyDSL "MXFP4
+ *                fp8-A" cases named in the split-K PR's test notes)
  *
  * Encodings are decoded from their bit fields through 256-entry tables built
  * once (OCP 8-bit floating point E4M3 "fn", OCP FP4 E2M1, E8M0, bfloat16).
@@ -47,7 +50,8 @@ enum {
     ORC_FP8_BLOCK128 = 2,
     ORC_MXFP8 = 3,
     ORC_MXFP4 = 4,
-    ORC_MXFP8_B32 = 5
+    ORC_MXFP8_B32 = 5,
+    ORC_MXFP4_FP8A = 6
 };
 
 /* ---------------------------------------------------------------- decoding */
@@ -143,6 +147,25 @@ typedef struct {
  * with a partial block (K < block) index correctly. */
 static int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
+/* e4m3 code [rows][K] times 2^(scale-127), one E8M0 per 32 K. */
+static double e4m3_e8m0_32(const void *X, const void *S, int64_t K, int64_t r, int64_t k)
+{
+    const int64_t kb = ceil_div(K, 32);
+    const double s = T_E8M0[((const uint8_t *)S)[r * kb + k / 32]];
+    return T_E4M3[((const uint8_t *)X)[r * K + k]] * s;
+}
+
+/* e2m1 codes packed two per byte [rows][K/2] (low nibble = even k) times
+ * 2^(scale-127), one E8M0 per 32 K. */
+static double e2m1_e8m0_32(const void *X, const void *S, int64_t K, int64_t r, int64_t k)
+{
+    const int64_t kb = ceil_div(K, 32);
+    const double s = T_E8M0[((const uint8_t *)S)[r * kb + k / 32]];
+    const uint8_t byte = ((const uint8_t *)X)[r * ceil_div(K, 2) + k / 2];
+    const unsigned nib = (k & 1) ? (byte >> 4) : (byte & 15u);
+    return T_E2M1[nib] * s;
+}
+
 /* Dequantised value of operand X (A or B) at (r, k).  `is_b` selects the
  * B-side block-scale indexing (128x128 blocks for FP8_BLOCK128). */
 static double dequant(const orc_job *j, int is_b, int64_t r, int64_t k)
@@ -166,18 +189,12 @@ static double dequant(const orc_job *j, int is_b, int64_t r, int64_t k)
         const double s = T_E8M0[((const uint8_t *)S)[r * kb + k / 128]];
         return T_E4M3[((const uint8_t *)X)[r * K + k]] * s;
     }
-    case ORC_MXFP8_B32: {
-        const int64_t kb = ceil_div(K, 32);
-        const double s = T_E8M0[((const uint8_t *)S)[r * kb + k / 32]];
-        return T_E4M3[((const uint8_t *)X)[r * K + k]] * s;
-    }
-    case ORC_MXFP4: {
-        const int64_t kb = ceil_div(K, 32);
-        const double s = T_E8M0[((const uint8_t *)S)[r * kb + k / 32]];
-        const uint8_t byte = ((const uint8_t *)X)[r * ceil_div(K, 2) + k / 2];
-        const unsigned nib = (k & 1) ? (byte >> 4) : (byte & 15u);
-        return T_E2M1[nib] * s;
-    }
+    case ORC_MXFP8_B32:
+        return e4m3_e8m0_32(X, S, K, r, k);
+    case ORC_MXFP4:
+        return e2m1_e8m0_32(X, S, K, r, k);
+    case ORC_MXFP4_FP8A: /* fp8 activations, fp4 weights */
+        return is_b ? e2m1_e8m0_32(X, S, K, r, k) : e4m3_e8m0_32(X, S, K, r, k);
     }
     return NAN;
 }
@@ -218,11 +235,11 @@ int orc_gemm(int mode, int64_t M, int64_t N, int64_t K,
              int tensor_scale, double *out, int threads)
 {
     ensure_tables();
-    if (mode < ORC_BF16 || mode > ORC_MXFP8_B32 || M < 0 || N < 0 || K < 0)
+    if (mode < ORC_BF16 || mode > ORC_MXFP4_FP8A || M < 0 || N < 0 || K < 0)
         return -1;
     if (k0 < 0 || k1 > K || k0 > k1)
         return -1;
-    if (mode == ORC_MXFP4 && (K % 2) != 0)
+    if ((mode == ORC_MXFP4 || mode == ORC_MXFP4_FP8A) && (K % 2) != 0)
         return -1;
     if (!rows)
         n_rows = M;
@@ -269,8 +286,8 @@ int orc_splitk_range(int mode, int64_t K, int S, int s, int64_t *k_begin, int64_
         per_unit = 64;
     else if (mode == ORC_MXFP4)
         per_unit = 256;
-    else if ((mode >= ORC_FP8_TENSOR && mode <= ORC_MXFP8) || mode == ORC_MXFP8_B32)
-        per_unit = 128;
+    else if ((mode >= ORC_FP8_TENSOR && mode <= ORC_MXFP8) || mode == ORC_MXFP8_B32 || mode == ORC_MXFP4_FP8A)
+        per_unit = 128; /* MXFP4_FP8A: one 128-byte slab of the fp8 A */
     else
         return -1;
     if (S < 1 || s < 0 || s >= S || K < 0 || K % per_unit != 0)
@@ -322,6 +339,34 @@ int orc_unshuffle_b(const uint8_t *in, int64_t N, int64_t Kb, uint8_t *B)
     return 0;
 }
 
+/*
+ * The MXFP4_FP8A weight image: B as packed fp4 bytes, N rows of Kb = K/2
+ * bytes, cut into blocks of 128 rows x 64 bytes (128 K of fp4), block
+ * (nb, u) at index nb * (Kb/64) + u, row r of the block at byte r*64, no
+ * swizzle.  (The kernel expands each block to e4m3 in shared memory itself.)
+ */
+int orc_block64_b(const uint8_t *B, int64_t N, int64_t Kb, uint8_t *out)
+{
+    if (N % 128 != 0 || Kb % 64 != 0 || N < 0 || Kb < 0)
+        return -1;
+    const int64_t U = Kb / 64;
+    for (int64_t n = 0; n < N; ++n)
+        for (int64_t u = 0; u < U; ++u)
+            memcpy(out + ((n / 128) * U + u) * 8192 + (n % 128) * 64, B + n * Kb + u * 64, 64);
+    return 0;
+}
+
+int orc_unblock64_b(const uint8_t *in, int64_t N, int64_t Kb, uint8_t *B)
+{
+    if (N % 128 != 0 || Kb % 64 != 0 || N < 0 || Kb < 0)
+        return -1;
+    const int64_t U = Kb / 64;
+    for (int64_t n = 0; n < N; ++n)
+        for (int64_t u = 0; u < U; ++u)
+            memcpy(B + n * Kb + u * 64, in + ((n / 128) * U + u) * 8192 + (n % 128) * 64, 64);
+    return 0;
+}
+
 /* --------------------------------------------------------- final rounding */
 
 /* bf16 round-to-nearest-even of an fp32 value, from its bit pattern. */
@@ -351,10 +396,13 @@ void orc_round_bf16(const double *in, int64_t n, uint16_t *out)
  * two for mxfp4), a 512-byte atom whose byte 16*(r%32) + 4*(r/32) + j holds
  * the E8M0 scale of row nb*128 + r for the 32-K block (u*atoms + a)*4 + j.
  * An mxfp8 scale covers 128 K, i.e. the four 32-K blocks of its slab.
- * sf is [N][K/128] (mxfp8) or [N][K/32] (mxfp4, mxfp8 with 32-K blocks).
+ * sf is [N][K/128] (mxfp8) or [N][K/32] (mxfp4, mxfp8 with 32-K blocks, and
+ * the fp4 weights of MXFP4_FP8A, whose slab is 128 K like MXFP8_B32's).
  */
 int orc_sf_image(int mode, const uint8_t *sf, int64_t N, int64_t K, uint8_t *out)
 {
+    if (mode == ORC_MXFP4_FP8A)
+        mode = ORC_MXFP8_B32;
     if ((mode != ORC_MXFP8 && mode != ORC_MXFP4 && mode != ORC_MXFP8_B32) || N % 128 != 0)
         return -1;
     const int64_t slab_k = mode == ORC_MXFP4 ? 256 : 128;

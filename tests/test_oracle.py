@@ -24,7 +24,16 @@ from tests import parity
 
 ml = pytest.importorskip("ml_dtypes")
 
-MODES = [oracle.BF16, oracle.FP8_TENSOR, oracle.FP8_BLOCK128, oracle.MXFP8, oracle.MXFP4, oracle.MXFP8_B32]
+MODES = [oracle.BF16, oracle.FP8_TENSOR, oracle.FP8_BLOCK128, oracle.MXFP8, oracle.MXFP4, oracle.MXFP8_B32,
+         oracle.MXFP4_FP8A]
+
+
+def _enc(mode, is_b):
+    """Encoding of one operand: MXFP4_FP8A has e4m3 activations (as MXFP8_B32)
+    and packed e2m1 weights (as MXFP4); every other mode uses one for both."""
+    if mode == oracle.MXFP4_FP8A:
+        return oracle.MXFP4 if is_b else oracle.MXFP8_B32
+    return mode
 
 
 # ------------------------------------------------------------ decode tables
@@ -77,6 +86,7 @@ def test_bf16_decode_matches_torch_all_patterns():
 
 def _frac_values(mode, X, S, rows, K, is_b):
     """Exact Fraction dequantised operand, decoded with ml_dtypes."""
+    mode = _enc(mode, is_b)
     if mode == oracle.BF16:
         v = X.view(np.uint16).view(ml.bfloat16).astype(np.float64)
     elif mode == oracle.MXFP4:
@@ -109,13 +119,10 @@ def _rand_case(mode, M, N, K, seed):
         A = inputs.to_bf16_bits(g.standard_normal((M, K)).astype(np.float32))
         B = inputs.to_bf16_bits(g.standard_normal((N, K)).astype(np.float32))
         return A, B, None, None
-    if mode == oracle.MXFP4:
-        A = g.integers(0, 256, (M, K // 2), dtype=np.uint8)
-        B = g.integers(0, 256, (N, K // 2), dtype=np.uint8)
-    else:
-        # all e4m3 codes except the two NaN patterns
-        pool = np.array([c for c in range(256) if (c & 0x7F) != 0x7F], np.uint8)
-        A, B = g.choice(pool, (M, K)), g.choice(pool, (N, K))
+    # all e4m3 codes except the two NaN patterns
+    pool = np.array([c for c in range(256) if (c & 0x7F) != 0x7F], np.uint8)
+    A = g.integers(0, 256, (M, K // 2), dtype=np.uint8) if _enc(mode, False) == oracle.MXFP4 else g.choice(pool, (M, K))
+    B = g.integers(0, 256, (N, K // 2), dtype=np.uint8) if _enc(mode, True) == oracle.MXFP4 else g.choice(pool, (N, K))
     if mode == oracle.FP8_TENSOR:
         return A, B, np.float32(g.uniform(0.01, 2)), np.float32(g.uniform(0.01, 2))
     if mode == oracle.FP8_BLOCK128:
@@ -182,6 +189,8 @@ ONE = {oracle.BF16: 0x3F80, oracle.FP8_TENSOR: 0x38, oracle.FP8_BLOCK128: 0x38,
 
 
 def _unit_scales(mode, rows, K):
+    if mode == oracle.MXFP4_FP8A:
+        return np.full((rows, K // 32), 127, np.uint8)
     if mode == oracle.FP8_TENSOR:
         return np.float32(1.0)
     if mode == oracle.FP8_BLOCK128:
@@ -194,6 +203,7 @@ def _unit_scales(mode, rows, K):
 
 
 def _const_operand(mode, rows, K, code):
+    """Constant operand in encoding `mode` (an operand encoding, see _enc)."""
     if mode == oracle.BF16:
         return np.full((rows, K), code, np.uint16)
     if mode == oracle.MXFP4:
@@ -202,6 +212,8 @@ def _const_operand(mode, rows, K, code):
 
 
 def _identity_operand(mode, M, K):
+    """Identity rows in the activation encoding of `mode`."""
+    mode = _enc(mode, False)
     X = np.zeros((M, K), np.uint16 if mode == oracle.BF16 else np.uint8)
     for m in range(M):
         X[m, m % K] = ONE[mode]
@@ -227,7 +239,7 @@ def test_identity_closed_form_is_exact(mode):
     expect = Bd[np.arange(M) % K, :]
     assert np.array_equal(y, expect)
     # and the decoded weight agrees with the independent library on raw codes
-    if mode == oracle.MXFP4:
+    if _enc(mode, True) == oracle.MXFP4:
         nib = np.empty((N, K), np.uint8)
         nib[:, 0::2], nib[:, 1::2] = B & 15, B >> 4
         vals = nib.view(ml.float4_e2m1fn).astype(np.float64)
@@ -241,8 +253,8 @@ def test_all_ones_closed_form(mode, K):
     if mode == oracle.MXFP4 and K % 256:
         pytest.skip("packed fp4 rows are cut in 128-byte (256-element) slabs")
     M, N = 3, 128
-    A = _const_operand(mode, M, K, ONE[mode])
-    B = _const_operand(mode, N, K, ONE[mode])
+    A = _const_operand(_enc(mode, False), M, K, ONE[_enc(mode, False)])
+    B = _const_operand(_enc(mode, True), N, K, ONE[_enc(mode, True)])
     a_s, b_s = _unit_scales(mode, M, K), _unit_scales(mode, N, K)
     if mode == oracle.FP8_BLOCK128:
         b_s = np.ones((1, K // 128), np.float32)
@@ -279,7 +291,8 @@ def test_mxfp4_nibble_order_low_is_even_k():
 
 # ----------------------------------------------------- split invariance
 
-@pytest.mark.parametrize("mode", [oracle.FP8_TENSOR, oracle.MXFP8, oracle.MXFP4, oracle.MXFP8_B32])
+@pytest.mark.parametrize("mode", [oracle.FP8_TENSOR, oracle.MXFP8, oracle.MXFP4, oracle.MXFP8_B32,
+                                  oracle.MXFP4_FP8A])
 def test_split_sums_are_exact(mode):
     name = oracle.MODE_NAMES[mode]
     M, N, K = 5, 128, 2048
@@ -313,7 +326,8 @@ def test_splitk_partition():
              for s in range(8)]
     assert sizes == [4, 4, 4, 4, 3, 3, 3, 3]
     for mode, K in [(oracle.BF16, 8192), (oracle.FP8_BLOCK128, 7168), (oracle.MXFP4, 7168),
-                    (oracle.MXFP8, 128), (oracle.MXFP8_B32, 7168)]:
+                    (oracle.MXFP8, 128), (oracle.MXFP8_B32, 7168), (oracle.MXFP4_FP8A, 7168),
+                    (oracle.MXFP4_FP8A, 384)]:
         for S in (1, 2, 3, 4, 8):
             rs = [oracle.splitk_range(mode, K, S, s) for s in range(S)]
             assert rs[0][0] == 0 and rs[-1][1] == K
@@ -359,6 +373,38 @@ def test_layout_spec(N, Kb):
         for kb in range(KB):
             slab = img[((n // 128) * KB + kb) * 16384:][:16384].reshape(128, 128)
             assert sorted(slab[n % 128].tolist()) == sorted(Bb[n, kb * 128:(kb + 1) * 128].tolist())
+
+
+@pytest.mark.parametrize("N,Kb", [(128, 64), (256, 192), (384, 3584)])
+def test_block64_layout_spec(N, Kb):
+    """The fp8-A x fp4-B weight image: 128-row x 64-byte blocks, unswizzled --
+    checked against a reshape/transpose restatement, its inverse, and a
+    bijection on unique 8-byte ids."""
+    g = np.random.default_rng(N + Kb)
+    Bb = g.integers(0, 256, (N, Kb), dtype=np.uint8)
+    img = oracle.block64_b(Bb, N, Kb)
+    indep = Bb.reshape(N // 128, 128, Kb // 64, 64).transpose(0, 2, 1, 3).reshape(-1)
+    assert np.array_equal(img, indep)
+    assert np.array_equal(oracle.unblock64_b(img, N, Kb), Bb)
+    ids = np.arange(N * Kb // 8, dtype=np.uint64)
+    moved = oracle.block64_b(ids.view(np.uint8).reshape(N, Kb), N, Kb).view(np.uint64)
+    assert np.array_equal(np.sort(moved), ids)
+
+
+def test_mixed_mode_equals_its_two_encodings():
+    """fp8-A x fp4-B is the sum of products of an mxfp8_b32 activation and an
+    mxfp4 weight: with the weight's fp4 values rewritten as the e4m3 codes of
+    the same numbers (every e2m1 value is an e4m3 value), the mxfp8_b32 oracle
+    gives the same bits; the weight's scale image equals mxfp8_b32's."""
+    M, N, K = 5, 256, 1024
+    A, B, a_s, b_s = inputs.operands("mxfp4_fp8a", M, N, K, 41, 42, 43)
+    y = oracle.gemm(oracle.MXFP4_FP8A, A, B, a_s, b_s, threads=2)
+    nib = np.empty((N, K), np.uint8)
+    nib[:, 0::2], nib[:, 1::2] = B & 15, B >> 4
+    B8 = nib.view(ml.float4_e2m1fn).astype(np.float32).astype(ml.float8_e4m3fn).view(np.uint8)
+    assert np.array_equal(oracle.table_e2m1()[nib], oracle.table_e4m3()[B8])
+    assert np.array_equal(y, oracle.gemm(oracle.MXFP8_B32, A, B8, a_s, b_s, threads=2))
+    assert np.array_equal(oracle.sf_image(oracle.MXFP4_FP8A, b_s, N, K), oracle.sf_image(oracle.MXFP8_B32, b_s, N, K))
 
 
 # ------------------------------------------------------------- inputs
