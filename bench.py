@@ -56,11 +56,19 @@ WORKLOADS = {
                                         idx=4, case_offset=2),
     "large_mxfp4_4096x16384x7168": dict(cases=[dict(mode="mxfp4", M=4096, N=16384, K=7168)], kind="large",
                                         idx=4, case_offset=5),
+    # fp8 activations against fp4 weights, on the MX shapes
+    "mxfp4_fp8a_decode_n16384_k7168": dict(cases=[dict(mode="mxfp4_fp8a", M=m, N=16384, K=7168) for m in (1, 16)],
+                                           kind="decode", idx=7),
+    "large_mxfp4_fp8a_4096x16384x7168": dict(cases=[dict(mode="mxfp4_fp8a", M=4096, N=16384, K=7168)],
+                                             kind="large", idx=7, case_offset=2),
 }
 DEFAULT_WORKLOAD = "fp8_tensor_decode_sweep_k7168"
 
 
-def elem_bytes(mode):
+def elem_bytes(mode, operand="a"):
+    """Bytes per element of operand "a" (activations) or "b" (weights)."""
+    if mode == "mxfp4_fp8a":
+        return 0.5 if operand == "b" else 1.0
     return {"bf16": 2.0, "mxfp4": 0.5}.get(mode, 1.0)
 
 
@@ -71,7 +79,7 @@ def scale_bytes(mode, M, N, K):
         return 4 * (M + N // 128) * (K // 128)
     if mode == "mxfp8":
         return (M + N) * (K // 128)
-    if mode in ("mxfp4", "mxfp8_b32"):
+    if mode in ("mxfp4", "mxfp8_b32", "mxfp4_fp8a"):
         return (M + N) * (K // 32)
     return 0
 
@@ -79,7 +87,7 @@ def scale_bytes(mode, M, N, K):
 def algo_bytes(c, n=None):
     """A + B + scales + Y bytes of one GEMM (n restricts to the first n weight rows)."""
     M, N, K, mode = c["M"], c["N"] if n is None else n, c["K"], c["mode"]
-    return int(M * K * elem_bytes(mode) + N * K * elem_bytes(mode) + scale_bytes(mode, M, N, K) + 2 * M * N)
+    return int(M * K * elem_bytes(mode, "a") + N * K * elem_bytes(mode, "b") + scale_bytes(mode, M, N, K) + 2 * M * N)
 
 
 def algo_flops(c, n=None):
@@ -164,7 +172,8 @@ class OracleSample:
         import oracle
         self.oracle = oracle
         self.orc = {"bf16": oracle.BF16, "fp8_tensor": oracle.FP8_TENSOR, "fp8_block128": oracle.FP8_BLOCK128,
-                    "mxfp8": oracle.MXFP8, "mxfp4": oracle.MXFP4, "mxfp8_b32": oracle.MXFP8_B32}
+                    "mxfp8": oracle.MXFP8, "mxfp4": oracle.MXFP4, "mxfp8_b32": oracle.MXFP8_B32,
+                    "mxfp4_fp8a": oracle.MXFP4_FP8A}
         self.wl, self.host_ops = wl, host_ops
         self.threads = os.cpu_count() or 1
         self.frac = 1.0 / 1024
@@ -182,7 +191,7 @@ class OracleSample:
             bs = b_s
             if c["mode"] == "fp8_block128":
                 bs = b_s[: (n + 127) // 128]
-            elif c["mode"] in ("mxfp8", "mxfp4", "mxfp8_b32"):
+            elif c["mode"] in ("mxfp8", "mxfp4", "mxfp8_b32", "mxfp4_fp8a"):
                 bs = b_s[:n]
             self.oracle.gemm(self.orc[c["mode"]], A, B[:n], a_s, bs, M=c["M"], N=n, K=c["K"],
                              threads=self.threads)
@@ -278,7 +287,7 @@ def main():
     off = wl.get("case_offset", 0)
     host_ops_fn = lambda: [case_operands(wl["idx"], i + off, c) for i, c in enumerate(wl["cases"])]  # noqa: E731
     dtype = {"bf16": "bf16", "fp8_tensor": "e4m3", "fp8_block128": "e4m3", "mxfp8": "e4m3",
-             "mxfp4": "e2m1", "mxfp8_b32": "e4m3"}[wl["cases"][0]["mode"]]
+             "mxfp4": "e2m1", "mxfp8_b32": "e4m3", "mxfp4_fp8a": "e4m3xe2m1"}[wl["cases"][0]["mode"]]
 
     if args.impl == "reference":
         if rank != 0:
@@ -434,7 +443,8 @@ def main():
         # a seconds-long loop of one contraction: the sustained bf16 figure,
         # times the nominal dense ratio of the operand type (fp8 4.5 and fp4
         # 13.5 vs bf16 2.25 PFLOP/s)
-        ratio = {"bf16": 1.0, "e4m3": 2.0, "e2m1": 6.0}[dtype]
+        # (fp8 x fp4 runs its MMAs as e4m3 x e4m3: the fp8 rate)
+        ratio = {"bf16": 1.0, "e4m3": 2.0, "e2m1": 6.0, "e4m3xe2m1": 2.0}[dtype]
         bound, peak = "tensor", ratio * float(peaks["bf16_tflops_sustained"])
         psrc = peaks_src + " bf16_tflops_sustained" + (
             " x %g (%s/bf16 nominal dense ratio)" % (ratio, dtype) if ratio != 1 else "")
@@ -556,8 +566,11 @@ def main():
     e2e_eager = whole_job_value(E, step_work, aggregate_ranks(e0.elapsed_time(e1), world, dist, dev), world,
                                 scale_u)
 
-    launches_per_step = sum((2 if x["S"] > 8 else 1) + (1 if x["plan"]["path"] == 1 and
-                                                        x["c"]["mode"] in ("mxfp8", "mxfp4", "mxfp8_b32") else 0)
+    # + the per-call A scale relayout of the large MX form (and the weight
+    # expansion of fp8 x fp4)
+    launches_per_step = sum((2 if x["S"] > 8 else 1) +
+                            (1 if x["plan"]["path"] == 1 and x["c"]["mode"] in ("mxfp8", "mxfp4", "mxfp8_b32") else 0) +
+                            (2 if x["plan"]["path"] == 1 and x["c"]["mode"] == "mxfp4_fp8a" else 0)
                             for x in cases)
 
     cpu = None

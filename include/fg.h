@@ -35,12 +35,13 @@
  *  - Only compute capability 10.3 devices are accepted
  *    (FG_ERR_UNSUPPORTED_ARCH otherwise).
  *  - Layouts are row-major.  A: [M][K] bf16 | e4m3 bytes | packed e2m1
- *    ([M][K/2] bytes, low nibble = even k).  B likewise [N][K].
+ *    ([M][K/2] bytes, low nibble = even k).  B likewise [N][K] (for
+ *    MXFP4_FP8A, A is e4m3 [M][K] and B packed e2m1 [N][K/2]).
  *    Y: [M][N] bf16.  Workspace: [split_k][M][N] fp32.
  *  - Shapes: N % 128 == 0; K * element bits / 8 must be a multiple of 128
- *    bytes (K % 64 for bf16, K % 128 for fp8, K % 256 for mxfp4); the
- *    128-K scale blocks of FP8_BLOCK128 / MXFP8 and the 32-K blocks of
- *    MXFP4 then divide K exactly.  M >= 0 (M == 0 is a no-op).
+ *    bytes (K % 64 for bf16, K % 128 for fp8 and MXFP4_FP8A, K % 256 for
+ *    mxfp4); the 128-K scale blocks of FP8_BLOCK128 / MXFP8 and the 32-K
+ *    blocks of MXFP4 then divide K exactly.  M >= 0 (M == 0 is a no-op).
  */
 #ifndef FG_H
 #define FG_H
@@ -77,7 +78,9 @@ typedef enum fg_mode {
   FG_FP8_BLOCK128 = 2, /* e4m3; a_s fp32 [M][K/128]; b_s fp32 [N/128][K/128]        */
   FG_MXFP8 = 3,        /* e4m3; E8M0 a_sf [M][K/128], b_sf [N][K/128]               */
   FG_MXFP4 = 4,        /* packed e2m1; E8M0 a_sf [M][K/32], b_sf [N][K/32]          */
-  FG_MXFP8_B32 = 5     /* e4m3; E8M0 a_sf [M][K/32], b_sf [N][K/32] (OCP MX block)  */
+  FG_MXFP8_B32 = 5,    /* e4m3; E8M0 a_sf [M][K/32], b_sf [N][K/32] (OCP MX block)  */
+  FG_MXFP4_FP8A = 6    /* A e4m3, E8M0 a_sf [M][K/32]; B packed e2m1, E8M0 b_sf     */
+                       /* [N][K/32] ("MXFP4 fp8-A": fp8 activations, fp4 weights)   */
 } fg_mode;
 
 /* fg_gemm flags */
@@ -101,11 +104,15 @@ typedef enum fg_mode {
  * nb*(Kb/128)+kb (16 KiB each); in a slab, 16-byte chunk c of row r sits at
  * byte r*128 + ((c ^ (r%8))*16) -- the image a 128-byte-swizzled K-major
  * tensor-core operand has in shared memory, so one pipeline stage of one
- * 128-row tile is one contiguous copy.
+ * 128-row tile is one contiguous copy.  MXFP4_FP8A instead keeps the packed
+ * fp4 bytes (Kb = K/2) in unswizzled blocks of 128 rows x 64 bytes (128 K),
+ * block (nb, kb) at index nb*(K/128)+kb, row r at byte r*64: the kernels
+ * expand each block to e4m3 (exactly: every e2m1 value is an e4m3 value).
  *
  * Scale image (sf): FP8_TENSOR: the fp32 b_s (16 bytes reserved);
  * FP8_BLOCK128: b_s fp32 [N/128][K/128] unchanged; MXFP8 / MXFP8_B32 /
- * MXFP4: for each 128-row tile and slab, 1 (8-bit) or 2 (MXFP4) atoms of 512
+ * MXFP4_FP8A (one atom per 128 K) / MXFP4: for each 128-row tile and slab,
+ * 1 (8-bit) or 2 (MXFP4) atoms of 512
  * bytes, atom byte 16*(r%32) + 4*(r/32) + j = the E8M0 of row r for the j-th
  * 32-K block the atom covers (an MXFP8 128-K scale repeated for its four
  * 32-K blocks); BF16: none.
@@ -197,13 +204,14 @@ FG_API fg_status fg_gemm_workspace_size(int mode, int64_t M, int64_t N, int64_t 
  * Y = dequant(A) . dequant(B)^T for the preshuffled weight `b`.
  *  A        device [M][K] codes (layout per mode, see top).
  *  a_scales FP8_TENSOR: device fp32 scalar; FP8_BLOCK128: fp32 [M][K/128];
- *           MXFP8: uint8 E8M0 [M][K/128]; MXFP4, MXFP8_B32: uint8 E8M0
- *           [M][K/32];
+ *           MXFP8: uint8 E8M0 [M][K/128]; MXFP4, MXFP8_B32, MXFP4_FP8A:
+ *           uint8 E8M0 [M][K/32];
  *           BF16: ignored (pass NULL).
  *  mode     must equal b->mode (FG_ERR_LAYOUT otherwise).
  *  split_k  0 = dispatch chooses; 1..16 = number of K splits.  Split s takes
  *           the contiguous run of 128-byte K slabs [s*q + min(s,r), ...) of
- *           length q + (s < r), q = U/S, r = U%S, U = Kb/128.
+ *           length q + (s < r), q = U/S, r = U%S, U = Kb/128 (for
+ *           MXFP4_FP8A, U = K/128: the slabs of the fp8 A).
  *  Y        device bf16 [M][N].
  *  workspace / workspace_bytes: as fg_gemm_workspace_size says; may be
  *           NULL when that is 0.  With FG_FLAG_DEFER_REDUCE (or a split

@@ -13,9 +13,9 @@ import torch
 HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(HERE, "_build", "libfg.so")
 
-FG_BF16, FG_FP8_TENSOR, FG_FP8_BLOCK128, FG_MXFP8, FG_MXFP4, FG_MXFP8_B32 = 0, 1, 2, 3, 4, 5
+FG_BF16, FG_FP8_TENSOR, FG_FP8_BLOCK128, FG_MXFP8, FG_MXFP4, FG_MXFP8_B32, FG_MXFP4_FP8A = 0, 1, 2, 3, 4, 5, 6
 MODES = {"bf16": FG_BF16, "fp8_tensor": FG_FP8_TENSOR, "fp8_block128": FG_FP8_BLOCK128,
-         "mxfp8": FG_MXFP8, "mxfp4": FG_MXFP4, "mxfp8_b32": FG_MXFP8_B32}
+         "mxfp8": FG_MXFP8, "mxfp4": FG_MXFP4, "mxfp8_b32": FG_MXFP8_B32, "mxfp4_fp8a": FG_MXFP4_FP8A}
 STATUS = ["FG_OK", "FG_ERR_INVALID_ARG", "FG_ERR_SHAPE", "FG_ERR_ALIGN", "FG_ERR_LAYOUT",
           "FG_ERR_WORKSPACE", "FG_ERR_UNSUPPORTED_ARCH", "FG_ERR_CUDA", "FG_ERR_TIMEOUT"]
 (FG_OK, FG_ERR_INVALID_ARG, FG_ERR_SHAPE, FG_ERR_ALIGN, FG_ERR_LAYOUT, FG_ERR_WORKSPACE,
@@ -156,7 +156,7 @@ def preshuffle_b(mode, B, b_scales=None, K=None, stream=None):
     mode = _mode(mode)
     N = B.shape[0]
     if K is None:
-        K = B.shape[1] * (2 if mode == FG_MXFP4 else 1)
+        K = B.shape[1] * (2 if mode in (FG_MXFP4, FG_MXFP4_FP8A) else 1)
     nb, ns = preshuffle_b_size(mode, N, K)
     data = torch.empty(nb, dtype=torch.uint8, device=B.device)
     sf = torch.empty(max(ns, 16), dtype=torch.uint8, device=B.device) if ns else None
@@ -169,7 +169,7 @@ def preshuffle_b(mode, B, b_scales=None, K=None, stream=None):
 def unshuffle_b(pb, stream=None):
     """Inverse relayout: (B bytes [N][Kb] uint8, scales in the caller layout or None)."""
     mode, N, K = pb.mode, pb.N, pb.K
-    kb = K * (2 if mode == FG_BF16 else 1) // (2 if mode == FG_MXFP4 else 1)
+    kb = K * (2 if mode == FG_BF16 else 1) // (2 if mode in (FG_MXFP4, FG_MXFP4_FP8A) else 1)
     B = torch.empty((N, kb), dtype=torch.uint8, device=pb.data.device)
     sc = None
     if mode == FG_FP8_TENSOR:
@@ -178,7 +178,7 @@ def unshuffle_b(pb, stream=None):
         sc = torch.empty((N // 128, K // 128), dtype=torch.float32, device=B.device)
     elif mode == FG_MXFP8:
         sc = torch.empty((N, K // 128), dtype=torch.uint8, device=B.device)
-    elif mode in (FG_MXFP4, FG_MXFP8_B32):
+    elif mode in (FG_MXFP4, FG_MXFP8_B32, FG_MXFP4_FP8A):
         sc = torch.empty((N, K // 32), dtype=torch.uint8, device=B.device)
     _check(lib().fg_unshuffle_b(ctypes.byref(pb.desc), _ptr(B), _ptr(sc), _stream(stream)))
     return B, sc

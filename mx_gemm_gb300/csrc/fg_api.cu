@@ -47,10 +47,10 @@ fg_status cuda_fail(cudaError_t e, const char* what) {
 
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
 
-bool mode_ok(int mode) { return mode >= FG_BF16 && mode <= FG_MXFP8_B32; }
+bool mode_ok(int mode) { return mode >= FG_BF16 && mode <= FG_MXFP4_FP8A; }
 
 const char* mode_name(int mode) {
-  static const char* names[] = {"bf16", "fp8_tensor", "fp8_block128", "mxfp8", "mxfp4", "mxfp8_b32"};
+  static const char* names[] = {"bf16", "fp8_tensor", "fp8_block128", "mxfp8", "mxfp4", "mxfp8_b32", "mxfp4_fp8a"};
   return mode_ok(mode) ? names[mode] : "?";
 }
 
@@ -120,10 +120,25 @@ uint64_t sf_image_bytes(int mode, int64_t N, int64_t K) {
     case FG_FP8_TENSOR: return 16;
     case FG_FP8_BLOCK128: return static_cast<uint64_t>(N / 128) * (K / 128) * 4;
     case FG_MXFP8:
-    case FG_MXFP8_B32: return static_cast<uint64_t>(N / 128) * (K / 128) * 512;
+    case FG_MXFP8_B32:
+    case FG_MXFP4_FP8A: return static_cast<uint64_t>(N / 128) * (K / 128) * 512;
     case FG_MXFP4: return static_cast<uint64_t>(N / 128) * (K / 256) * 2 * 512;
     default: return 0;
   }
+}
+
+// Workspace of the large-M MX kernel: A's scale atoms relaid per call and,
+// for MXFP4_FP8A, after them (256-byte aligned) the weights expanded to e4m3
+// (N*K bytes).  *expanded_at = that offset (0 when there is none).
+uint64_t large_mx_workspace(int mode, int64_t M, int64_t N, int64_t K, uint64_t* expanded_at) {
+  const uint64_t a_sf = sf_rows_image_bytes(mode, M, K);
+  if (mode != FG_MXFP4_FP8A) {
+    if (expanded_at) *expanded_at = 0;
+    return a_sf;
+  }
+  const uint64_t at = (a_sf + 255) / 256 * 256;
+  if (expanded_at) *expanded_at = at;
+  return at + static_cast<uint64_t>(N) * K;
 }
 
 // ------------------------------------------------------------ dispatch
@@ -372,7 +387,7 @@ fg_status fg_preshuffle_b_size(int mode, int64_t N, int64_t K, uint64_t* b_bytes
   if (!b_bytes || !sf_bytes) return fail(FG_ERR_INVALID_ARG, "null output pointer");
   fg_status s = check_nk(mode, N, K);
   if (s != FG_OK) return s;
-  *b_bytes = static_cast<uint64_t>(N) * row_bytes(mode, K);
+  *b_bytes = static_cast<uint64_t>(N) * b_row_bytes(mode, K);
   *sf_bytes = sf_image_bytes(mode, N, K);
   return FG_OK;
 }
@@ -398,7 +413,9 @@ fg_status fg_preshuffle_b(int mode, const void* B, const void* b_scales, int64_t
   if (b0 < i0 + need_b && i0 < b0 + need_b) return fail(FG_ERR_INVALID_ARG, "B and its image overlap");
   if ((s = check_arch()) != FG_OK) return s;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  cudaError_t e = launch_relayout_b(b0, static_cast<uint8_t*>(b_image), N, row_bytes(mode, K), false, st);
+  cudaError_t e = mode == FG_MXFP4_FP8A
+                      ? launch_block64_b(b0, static_cast<uint8_t*>(b_image), N, b_row_bytes(mode, K), false, st)
+                      : launch_relayout_b(b0, static_cast<uint8_t*>(b_image), N, row_bytes(mode, K), false, st);
   if (e != cudaSuccess) return cuda_fail(e, "weight relayout launch");
   if (mode == FG_FP8_TENSOR || mode == FG_FP8_BLOCK128) {
     e = cudaMemcpyAsync(sf_image, b_scales, mode == FG_FP8_TENSOR ? 4 : need_sf, cudaMemcpyDeviceToDevice, st);
@@ -432,8 +449,12 @@ fg_status fg_unshuffle_b(const fg_bshuf* desc, void* B_out, void* b_scales_out, 
   if (!aligned(B_out, 16)) return fail(FG_ERR_ALIGN, "B_out must be 16-byte aligned");
   if ((s = check_arch()) != FG_OK) return s;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  cudaError_t e = launch_relayout_b(static_cast<const uint8_t*>(desc->data), static_cast<uint8_t*>(B_out), desc->N,
-                                    row_bytes(desc->mode, desc->K), true, st);
+  cudaError_t e =
+      desc->mode == FG_MXFP4_FP8A
+          ? launch_block64_b(static_cast<const uint8_t*>(desc->data), static_cast<uint8_t*>(B_out), desc->N,
+                             b_row_bytes(desc->mode, desc->K), true, st)
+          : launch_relayout_b(static_cast<const uint8_t*>(desc->data), static_cast<uint8_t*>(B_out), desc->N,
+                              row_bytes(desc->mode, desc->K), true, st);
   if (e != cudaSuccess) return cuda_fail(e, "inverse relayout launch");
   if (b_scales_out && desc->sf) {
     if (desc->mode == FG_FP8_TENSOR || desc->mode == FG_FP8_BLOCK128) {
@@ -465,7 +486,7 @@ fg_status fg_gemm_workspace_size(int mode, int64_t M, int64_t N, int64_t K, int 
   if (s != FG_OK) return s;
   if (plan.path == 1) {
     const int64_t tiles = ((M + plan.tile_m - 1) / plan.tile_m) * (N / 256 + (N % 256 ? 1 : 0));
-    *bytes = is_mx(mode) ? sf_rows_image_bytes(mode, M, K)
+    *bytes = is_mx(mode) ? large_mx_workspace(mode, M, N, K, nullptr)
                          : large_streamk_plan(mode, tiles, row_bytes(mode, K) / 128, plan.ctas, nullptr,
                                               plan.tile_m == 256);
   }
@@ -509,10 +530,11 @@ fg_status fg_gemm(const void* A, const void* a_scales, int64_t M, const fg_bshuf
   }
   if (plan.path == 1 && mx) {
     // the large-M MX kernel reads A's scales as 512-byte atoms relaid per call
-    const uint64_t need = sf_rows_image_bytes(mode, M, K);
+    // (and MXFP4_FP8A's weights expanded to e4m3)
+    const uint64_t need = large_mx_workspace(mode, M, N, K, nullptr);
     if (!workspace || workspace_bytes < need)
-      return fail(FG_ERR_WORKSPACE, "large-M %s needs a %llu-byte workspace for the A scale image", mode_name(mode),
-                  (unsigned long long)need);
+      return fail(FG_ERR_WORKSPACE, "large-M %s needs a %llu-byte workspace for the A scale image%s", mode_name(mode),
+                  (unsigned long long)need, mode == FG_MXFP4_FP8A ? " and the expanded weights" : "");
     if (!aligned(workspace, 16)) return fail(FG_ERR_ALIGN, "workspace must be 16-byte aligned");
   }
   if ((s = check_arch()) != FG_OK) return s;
@@ -554,13 +576,25 @@ fg_status fg_gemm(const void* A, const void* a_scales, int64_t M, const fg_bshuf
         large_streamk_plan(mode, 0, 0, 0, &p, false);  // all tiles whole
       }
     }
+    int kernel_mode = mode;
     if (mx) {
       e = launch_relayout_sf_rows(mode, static_cast<const uint8_t*>(a_scales), static_cast<uint8_t*>(workspace), M, K,
                                   st);
       if (e != cudaSuccess) return cuda_fail(e, "A scale relayout launch");
       p.a_sf = static_cast<const uint8_t*>(workspace);
     }
-    e = launch_large(mode, tmap, p, plan.ctas, st);
+    if (mode == FG_MXFP4_FP8A) {
+      // the fp4 weights expanded once per call to the e4m3 image of the same
+      // values; from there on this is the e4m3 x e4m3 32-K-block GEMM
+      uint64_t at = 0;
+      large_mx_workspace(mode, M, N, K, &at);
+      uint8_t* expanded = static_cast<uint8_t*>(workspace) + at;
+      e = launch_expand_fp4_e4m3(static_cast<const uint8_t*>(b->data), expanded, N, K, st);
+      if (e != cudaSuccess) return cuda_fail(e, "weight expansion launch");
+      p.b_img = expanded;
+      kernel_mode = kMXFP8B32;
+    }
+    e = launch_large(kernel_mode, tmap, p, plan.ctas, st);
     if (e != cudaSuccess) return cuda_fail(e, "large-M kernel launch");
     return FG_OK;
   }

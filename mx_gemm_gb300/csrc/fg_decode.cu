@@ -17,7 +17,9 @@
 //             and tcgen05.mma, and commits stage releases;
 //   warps 2-5 for MX, first build the token scale atoms of each stage from
 //             the caller's E8M0 bytes (ahead of the MMA, one arrival per warp
-//             on the stage's full barrier); then
+//             on the stage's full barrier) -- for fp8 activations against
+//             fp4 weights they also expand the stage's packed fp4 weight
+//             blocks into the e4m3 tile the MMA reads; then
 //             epilogue: TMEM -> registers -> fp32 partials (split > 1) or
 //             scaled bf16 Y (split == 1).  For FP8_BLOCK128 they also run
 //             the per-128-K promotion: each K slab (one 128-K scale block)
@@ -76,12 +78,17 @@ constexpr int kTokRows = 16;
 
 template <int MODE, int SPS, int STAGES>
 struct DCfg {
-  static constexpr int APS = MODE == kMXFP4 ? 2 : ((MODE == kMXFP8 || MODE == kMXFP8B32) ? 1 : 0);
+  static constexpr int APS = MODE == kMXFP4 ? 2 : (is_mx(MODE) ? 1 : 0);
+  // fp8 activations x fp4 weights: the weight arrives as packed fp4 blocks
+  // (128 rows x 64 bytes per slab) in a staging area and is expanded to e4m3
+  static constexpr bool EXPAND = MODE == kMXFP4FP8A;
   static constexpr int B_BYTES = SPS * kSlabBytes;
   static constexpr int A_BYTES = SPS * kTokSlabBytes;
   static constexpr int SFW_BYTES = SPS * APS * 512;
   static constexpr int SFT_BYTES = APS ? SPS * APS * 256 + 256 : 0;
-  static constexpr int STAGE_RAW = B_BYTES + A_BYTES + SFW_BYTES + SFT_BYTES;
+  static constexpr int RAW_OFF = B_BYTES + A_BYTES + SFW_BYTES + SFT_BYTES;
+  static constexpr int RAW_BYTES = EXPAND ? SPS * 8192 : 0;
+  static constexpr int STAGE_RAW = RAW_OFF + RAW_BYTES;
   static constexpr int STAGE_BYTES = (STAGE_RAW + 1023) / 1024 * 1024;
   static constexpr int NBUF = 8;  // blockscale TMEM partial buffers
   static constexpr int SF_COLS = SPS * APS * 4;  // TMEM columns per operand per stage
@@ -113,6 +120,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   __shared__ __align__(8) uint64_t pempty_bar[C::NBUF];
   __shared__ __align__(8) uint64_t acc_bar, stall_bar, drain_bar;
   __shared__ __align__(8) uint64_t ready_bar, recv_bar;  // fused split-K reduce
+  __shared__ __align__(8) uint64_t raw_bar[STAGES];      // packed fp4 weights landed (EXPAND)
   __shared__ uint32_t tmem_base_sh;
   __shared__ int abort_sh, issued_sh, consumed_sh, mma_any_sh;
 
@@ -133,6 +141,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int i = 0; i < STAGES; ++i) {
       mbar_init(&full_bar[i], C::APS ? 5 : 1);  // MX: + one arrival per scale-building warp
       mbar_init(&empty_bar[i], 1);
+      mbar_init(&raw_bar[i], 1);
     }
     for (int i = 0; i < C::NBUF; ++i) {
       mbar_init(&pfull_bar[i], 1);
@@ -182,10 +191,17 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int nsl = min(SPS, nslab - ub);
       uint8_t* st = smem + slot * C::STAGE_BYTES;
       if (lane == 0) {
-        const uint32_t bytes = nsl * (kSlabBytes + kTokSlabBytes + C::APS * 512);
-        mbar_arrive_expect_tx(&full_bar[slot], bytes);
-        bulk_g2s(st, p.b_img + (static_cast<size_t>(nt) * p.KB + u0 + ub) * kSlabBytes, nsl * kSlabBytes,
-                 &full_bar[slot]);
+        if (C::EXPAND) {
+          // packed fp4 blocks into the staging area, on their own barrier
+          mbar_arrive_expect_tx(&raw_bar[slot], nsl * 8192);
+          bulk_g2s(st + C::RAW_OFF, p.b_img + (static_cast<size_t>(nt) * p.KB + u0 + ub) * 8192, nsl * 8192,
+                   &raw_bar[slot]);
+          mbar_arrive_expect_tx(&full_bar[slot], nsl * (kTokSlabBytes + C::APS * 512));
+        } else {
+          mbar_arrive_expect_tx(&full_bar[slot], nsl * (kSlabBytes + kTokSlabBytes + C::APS * 512));
+          bulk_g2s(st, p.b_img + (static_cast<size_t>(nt) * p.KB + u0 + ub) * kSlabBytes, nsl * kSlabBytes,
+                   &full_bar[slot]);
+        }
         if (C::APS)
           bulk_g2s(st + C::B_BYTES + C::A_BYTES,
                    p.b_sf + (static_cast<size_t>(nt) * p.KB + u0 + ub) * C::APS * 512, nsl * C::APS * 512,
@@ -283,7 +299,7 @@ __global__ void __launch_bounds__(kThreads, 1)
               mma_f16(d, adesc, bdesc, idesc_bf16(128, kTokRows), acc);
             } else if (MODE == kTensor || MODE == kBlock) {
               mma_f8f6f4(d, adesc, bdesc, idesc_e4m3(128, kTokRows), acc);
-            } else if (MODE == kMXFP8 || MODE == kMXFP8B32) {
+            } else if (MODE == kMXFP8 || MODE == kMXFP8B32 || MODE == kMXFP4FP8A) {
               mma_mxf8f6f4(d, adesc, bdesc, mx_idesc(MODE, j), tmem + sfw_col + 4 * v, tmem + sft_col + 4 * v, acc);
             } else {
               const int t = v * 2 + (j >> 1);
@@ -331,7 +347,29 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint8_t* asf = static_cast<const uint8_t*>(p.a_scales);
       const int et = threadIdx.x - 64;  // 0..127
       bool okb = true;
+      // One word per (atom t, token row m) of a stage, at most one per thread
+      // (SPS * APS * 16 <= 128): the four E8M0 bytes of the atom's 32-K
+      // blocks.  The next stage's word is loaded while this stage is
+      // processed, so the global-load latency is not paid stage after stage.
+      auto tok_sf = [&](int it) -> uint32_t {
+        const int nsl = min(SPS, nslab - it * SPS);
+        if (et >= nsl * C::APS * kTokRows) return 0u;
+        const int t = et / kTokRows, m = et % kTokRows;
+        const int row = mt * kTokRows + m;
+        if (row >= p.M) return 0x7F7F7F7Fu;  // 2^0 for padded rows (their values are zero)
+        const int q32 = ((u0 + it * SPS) * C::APS + t) * 4;  // first 32-K block of the atom
+        if (MODE != kMXFP8) {  // one scale per 32-K block
+          const uint8_t* src = asf + static_cast<size_t>(row) * (p.K / 32) + q32;
+          // K % 128 == 0 keeps the offset a multiple of 4: one word load
+          // unless the caller's scale array itself is not 4-byte aligned
+          if ((reinterpret_cast<uintptr_t>(asf) & 3u) == 0) return __ldg(reinterpret_cast<const uint32_t*>(src));
+          return static_cast<uint32_t>(src[0]) | (static_cast<uint32_t>(src[1]) << 8) |
+                 (static_cast<uint32_t>(src[2]) << 16) | (static_cast<uint32_t>(src[3]) << 24);
+        }
+        return static_cast<uint32_t>(asf[static_cast<size_t>(row) * (p.K / 128) + (q32 >> 2)]) * 0x01010101u;
+      };
       pdl_wait();
+      uint32_t wv_next = tok_sf(0);
       for (int it = 0; it < niter; ++it) {
         const int slot = it % STAGES;
         const bool w = mbar_wait(&empty_bar[slot], ((it / STAGES) & 1) ^ 1u, T, p.err, 8);
@@ -341,23 +379,35 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         const int ub = it * SPS;
         const int nsl = min(SPS, nslab - ub);
+        const uint32_t wv = wv_next;
+        if (it + 1 < niter) wv_next = tok_sf(it + 1);
         uint8_t* sft = smem + slot * C::STAGE_BYTES + C::B_BYTES + C::A_BYTES + C::SFW_BYTES;
-        for (int idx = et; idx < nsl * C::APS * kTokRows; idx += 128) {
-          const int t = idx / kTokRows, m = idx % kTokRows;
-          const int row = mt * kTokRows + m;
-          uint32_t wv = 0x7F7F7F7Fu;  // 2^0 for padded rows (their values are zero)
-          if (row < p.M) {
-            const int q32 = ((u0 + ub) * C::APS + t) * 4;  // first 32-K block of the atom
-            if (MODE != kMXFP8) {   // one scale per 32-K block
-              const uint8_t* src = asf + static_cast<size_t>(row) * (p.K / 32) + q32;
-              wv = static_cast<uint32_t>(src[0]) | (static_cast<uint32_t>(src[1]) << 8) |
-                   (static_cast<uint32_t>(src[2]) << 16) | (static_cast<uint32_t>(src[3]) << 24);
-            } else {
-              const uint32_t c = asf[static_cast<size_t>(row) * (p.K / 128) + (q32 >> 2)];
-              wv = c * 0x01010101u;
+        if (et < nsl * C::APS * kTokRows)
+          *reinterpret_cast<uint32_t*>(sft + (et / kTokRows) * 256 + (et % kTokRows) * 16) = wv;
+        if (C::EXPAND) {
+          // Expand the stage's packed fp4 weight blocks (row r: 64 bytes, four
+          // 16-byte chunks of 32 codes) into the 128-byte-swizzled e4m3 tile:
+          // chunk c4 of row r becomes e4m3 chunks 2*c4 and 2*c4+1, stored at
+          // r*128 + ((c ^ (r%8))*16) like every other weight tile.
+          const bool wr = mbar_wait(&raw_bar[slot], (it / STAGES) & 1, T, p.err, 12);
+          if (!__all_sync(0xffffffffu, wr)) {
+            okb = false;
+            break;
+          }
+          const uint8_t* raw = smem + slot * C::STAGE_BYTES + C::RAW_OFF;
+          uint8_t* tile = smem + slot * C::STAGE_BYTES;
+          for (int v = 0; v < nsl; ++v) {
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+              const int c = q * 128 + et;  // chunk of the block: row c/4, quarter c%4
+              const int r = c >> 2, c4 = c & 3;
+              uint4 lo, hi;
+              e2m1x32_to_e4m3x32(*reinterpret_cast<const uint4*>(raw + v * 8192 + c * 16), lo, hi);
+              uint8_t* row = tile + v * kSlabBytes + r * 128;
+              *reinterpret_cast<uint4*>(row + (((2 * c4) ^ (r & 7)) << 4)) = lo;
+              *reinterpret_cast<uint4*>(row + (((2 * c4 + 1) ^ (r & 7)) << 4)) = hi;
             }
           }
-          *reinterpret_cast<uint32_t*>(sft + t * 256 + m * 16) = wv;
         }
         fence_proxy_async_smem();
         __syncwarp();
@@ -507,8 +557,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     // Let every copy this CTA started land before its shared memory goes
     // away, and every MMA it issued finish before TMEM is released.
     if (threadIdx.x == 0) {
-      for (int it = consumed_sh; it < issued_sh; ++it)
+      for (int it = consumed_sh; it < issued_sh; ++it) {
+        if (C::EXPAND) mbar_wait(&raw_bar[it % STAGES], (it / STAGES) & 1, T, nullptr, 0);
         mbar_wait(&full_bar[it % STAGES], (it / STAGES) & 1, T, nullptr, 0);
+      }
     }
   }
   __syncthreads();
@@ -560,11 +612,20 @@ cudaError_t launch_one(const CUtensorMap& tmap_a, const DecodeParams& p, dim3 gr
   X(MODE, 2, 3)                    \
   X(MODE, 2, 5)                    \
   X(MODE, 4, 2)
+#define FG_DECODE_CONFIGS_EXPAND(X, MODE) \
+  X(MODE, 1, 4)                           \
+  X(MODE, 1, 5)                           \
+  X(MODE, 1, 6)                           \
+  X(MODE, 1, 8)                           \
+  X(MODE, 2, 3)                           \
+  X(MODE, 4, 2)
 
 }  // namespace
 
 bool decode_config_supported(const DecodeConfig& c) {
-  if (c.mode < kBF16 || c.mode > kMXFP8B32) return false;
+  if (c.mode < kBF16 || c.mode > kMXFP4FP8A) return false;
+  // with its fp4 staging area, 2 slabs x 5 stages exceed shared memory
+  if (c.mode == kMXFP4FP8A && c.sps == 2 && c.stages == 5) return false;
   return (c.sps == 1 && (c.stages == 4 || c.stages == 5 || c.stages == 6 || c.stages == 8)) ||
          (c.sps == 2 && (c.stages == 3 || c.stages == 5)) || (c.sps == 4 && c.stages == 2);
 }
@@ -579,6 +640,7 @@ cudaError_t launch_decode(const DecodeConfig& c, const CUtensorMap& tmap_a, cons
   FG_DECODE_CONFIGS(FG_TRY, kMXFP8)
   FG_DECODE_CONFIGS(FG_TRY, kMXFP4)
   FG_DECODE_CONFIGS(FG_TRY, kMXFP8B32)
+  FG_DECODE_CONFIGS_EXPAND(FG_TRY, kMXFP4FP8A)
 #undef FG_TRY
   return cudaErrorInvalidValue;
 }

@@ -8,14 +8,18 @@
 
 namespace fg {
 
-enum Mode : int { kBF16 = 0, kTensor = 1, kBlock = 2, kMXFP8 = 3, kMXFP4 = 4, kMXFP8B32 = 5 };
+// kMXFP4FP8A: e4m3 activations with 32-K E8M0 scales against packed e2m1
+// weights with 32-K E8M0 scales.
+enum Mode : int { kBF16 = 0, kTensor = 1, kBlock = 2, kMXFP8 = 3, kMXFP4 = 4, kMXFP8B32 = 5, kMXFP4FP8A = 6 };
 
-inline bool is_mx(int mode) { return mode == kMXFP8 || mode == kMXFP4 || mode == kMXFP8B32; }
+constexpr bool is_mx(int mode) { return mode == kMXFP8 || mode == kMXFP4 || mode == kMXFP8B32 || mode == kMXFP4FP8A; }
 // MX scale columns per row: one per 128 K (mxfp8) or per 32 K.
 inline int64_t mx_sf_cols(int mode, int64_t K) { return mode == kMXFP8 ? K / 128 : K / 32; }
 
+// Bytes per row of A (and of B, except for kMXFP4FP8A's packed fp4 weights).
 inline int elem_bits(int mode) { return mode == kBF16 ? 16 : (mode == kMXFP4 ? 4 : 8); }
 inline int64_t row_bytes(int mode, int64_t K) { return K * elem_bits(mode) / 8; }
+inline int64_t b_row_bytes(int mode, int64_t K) { return mode == kMXFP4FP8A ? K / 2 : row_bytes(mode, K); }
 // 512-byte scale-factor atoms per 128-byte K slab of the weight image.
 inline int sf_atoms_per_slab(int mode) { return mode == kMXFP4 ? 2 : (is_mx(mode) ? 1 : 0); }
 
@@ -89,6 +93,12 @@ cudaError_t launch_relayout_b(const uint8_t* src, uint8_t* dst, int64_t N, int64
                               cudaStream_t stream);
 cudaError_t launch_relayout_sf(int mode, const uint8_t* src, uint8_t* dst, int64_t N, int64_t K, bool inverse,
                                cudaStream_t stream);
+// kMXFP4FP8A weight image: packed fp4 [N][Kb] <-> 128-row x 64-byte blocks.
+cudaError_t launch_block64_b(const uint8_t* src, uint8_t* dst, int64_t N, int64_t Kb, bool inverse,
+                             cudaStream_t stream);
+// kMXFP4FP8A weight image -> the e4m3 weight image (128-byte-swizzled slabs)
+// of the same values, N*K bytes.
+cudaError_t launch_expand_fp4_e4m3(const uint8_t* src, uint8_t* dst, int64_t N, int64_t K, cudaStream_t stream);
 uint64_t sf_rows_image_bytes(int mode, int64_t rows, int64_t K);
 cudaError_t launch_relayout_sf_rows(int mode, const uint8_t* src, uint8_t* dst, int64_t rows, int64_t K,
                                     cudaStream_t stream);

@@ -332,6 +332,33 @@ __device__ __forceinline__ bool wait_flag_eq(const unsigned long long* flag, uns
   return true;
 }
 
+// ---------------------------------------------------- fp4 -> fp8 codes
+
+// The four e2m1 codes in the low 16 bits of w (code i in bits 4i..4i+3) as
+// four e4m3 codes (code i in byte i) of the same values: every e2m1 value is
+// an e4m3 value.  Magnitudes 0, 0.5, 1, 1.5, 2, 3, 4, 6 are e4m3 codes 0x00,
+// 0x30, 0x38, 0x3C, 0x40, 0x44, 0x48, 0x4C (selected by the 3 low bits of
+// each code); the sign moves from bit 3 of the code to bit 7 of the byte.
+__device__ __forceinline__ uint32_t e2m1x4_to_e4m3x4(uint32_t w) {
+  const uint32_t mag = __byte_perm(0x3C383000u, 0x4C484440u, w & 0x7777u);
+  uint32_t sg = w & 0x8888u;                 // sign of code i at bit 4i+3
+  sg = (sg | (sg << 8)) & 0x00880088u;       // codes 2, 3 to the upper half
+  sg = (sg | (sg << 4)) & 0x08080808u;       // code i's sign at bit 8i+3
+  return mag | (sg << 4);
+}
+
+// 16 bytes of packed e2m1 (32 codes, low nibble first) as 32 e4m3 bytes.
+__device__ __forceinline__ void e2m1x32_to_e4m3x32(uint4 q, uint4& lo, uint4& hi) {
+  lo.x = e2m1x4_to_e4m3x4(q.x);
+  lo.y = e2m1x4_to_e4m3x4(q.x >> 16);
+  lo.z = e2m1x4_to_e4m3x4(q.y);
+  lo.w = e2m1x4_to_e4m3x4(q.y >> 16);
+  hi.x = e2m1x4_to_e4m3x4(q.z);
+  hi.y = e2m1x4_to_e4m3x4(q.z >> 16);
+  hi.z = e2m1x4_to_e4m3x4(q.w);
+  hi.w = e2m1x4_to_e4m3x4(q.w >> 16);
+}
+
 // ------------------------------------------------------------- descriptors
 
 // Shared-memory matrix descriptor for a K-major operand stored in the

@@ -8,7 +8,8 @@ import oracle
 from tests import parity
 
 ORC = {"bf16": oracle.BF16, "fp8_tensor": oracle.FP8_TENSOR, "fp8_block128": oracle.FP8_BLOCK128,
-       "mxfp8": oracle.MXFP8, "mxfp4": oracle.MXFP4, "mxfp8_b32": oracle.MXFP8_B32}
+       "mxfp8": oracle.MXFP8, "mxfp4": oracle.MXFP4, "mxfp8_b32": oracle.MXFP8_B32,
+       "mxfp4_fp8a": oracle.MXFP4_FP8A}
 
 
 def dev(x):

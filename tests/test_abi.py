@@ -57,6 +57,8 @@ def test_version_and_status_names(fg):
     ("mxfp8", 16384, 7168, 16384 * 7168, 128 * 56 * 512),
     ("mxfp4", 16384, 7168, 16384 * 3584, 128 * 28 * 1024),
     ("mxfp8_b32", 16384, 7168, 16384 * 7168, 128 * 56 * 512),
+    ("mxfp4_fp8a", 16384, 7168, 16384 * 3584, 128 * 56 * 512),
+    ("mxfp4_fp8a", 256, 384, 256 * 192, 2 * 3 * 512),
 ])
 def test_preshuffle_sizes(fg, mode, N, K, b, sf):
     assert fg.preshuffle_b_size(mode, N, K) == (b, sf)

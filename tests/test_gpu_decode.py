@@ -15,7 +15,7 @@ from tests.gpu_util import Case, dev, host, y_to_f64
 
 pytestmark = pytest.mark.gpu
 
-MODES = ["bf16", "fp8_tensor", "fp8_block128", "mxfp8", "mxfp4", "mxfp8_b32"]
+MODES = ["bf16", "fp8_tensor", "fp8_block128", "mxfp8", "mxfp4", "mxfp8_b32", "mxfp4_fp8a"]
 
 
 def _slabs(mode, K):
@@ -94,6 +94,8 @@ def test_every_pipeline_config(mode, cfg, monkeypatch):
     FG_DECODE_CONFIG hook: ragged token tile, splits 1 and 3 (three CTAs with
     unequal K shares and unequal row counts), stage buffers reused several
     times, every output against the oracle."""
+    if mode == "mxfp4_fp8a" and cfg == "2,5":
+        pytest.skip("with its fp4 staging area this pipeline exceeds shared memory (refused)")
     monkeypatch.setenv("FG_DECODE_CONFIG", cfg)
     M, N, K = 5, 256, 3072
     c = Case(mode, *inputs.operands(mode, M, N, K, 700, 701, 702))
@@ -105,8 +107,25 @@ def test_every_pipeline_config(mode, cfg, monkeypatch):
     assert fg.get_error() == fg.FG_OK
 
 
+@pytest.mark.parametrize("mode", ["mxfp8", "mxfp4", "mxfp8_b32", "mxfp4_fp8a"])
+def test_unaligned_mx_activation_scales(mode):
+    """E8M0 activation scales passed at an odd address (a byte view one past
+    an allocation's start) are read byte by byte: same result as aligned."""
+    M, N, K = 5, 256, 2048
+    c = Case(mode, *inputs.operands(mode, M, N, K, 801, 802, 803))
+    buf = torch.zeros(c.a_s.size + 16, dtype=torch.uint8, device="cuda")
+    odd = buf[1:1 + c.a_s.size]
+    odd.copy_(dev(np.ascontiguousarray(c.a_s).reshape(-1)))
+    assert odd.data_ptr() % 4 != 0
+    for S in (1, 2):
+        y = y_to_f64(fg.gemm(c.dA, c.pb, odd.view(c.a_s.shape), split_k=S))
+        parity.assert_y_close(y, c.ref(), f"{mode} unaligned scales S={S}")
+        assert np.array_equal(y, y_to_f64(c.gemm(split_k=S)))
+    assert fg.get_error() == fg.FG_OK
+
+
 ONE = {"bf16": 0x3F80, "fp8_tensor": 0x38, "fp8_block128": 0x38, "mxfp8": 0x38, "mxfp4": 0x2,
-       "mxfp8_b32": 0x38}
+       "mxfp8_b32": 0x38, "mxfp4_fp8a": 0x38}   # the activation's code for 1.0
 
 
 def _unit_a_scales(mode, M, K):
@@ -114,7 +133,8 @@ def _unit_a_scales(mode, M, K):
             "fp8_block128": np.ones((M, K // 128), np.float32),
             "mxfp8": np.full((M, K // 128), 127, np.uint8),
             "mxfp4": np.full((M, K // 32), 127, np.uint8),
-            "mxfp8_b32": np.full((M, K // 32), 127, np.uint8)}.get(mode)
+            "mxfp8_b32": np.full((M, K // 32), 127, np.uint8),
+            "mxfp4_fp8a": np.full((M, K // 32), 127, np.uint8)}.get(mode)
 
 
 @pytest.mark.parametrize("mode", MODES)
@@ -146,9 +166,12 @@ def test_all_ones_is_exact(mode):
     A = np.full((M, K if mode != "mxfp4" else K // 2),
                 ONE[mode] if mode != "mxfp4" else 0x22, np.uint16 if mode == "bf16" else np.uint8)
     B = np.full((N, A.shape[1]), A.flat[0], A.dtype)
+    if mode == "mxfp4_fp8a":
+        B = np.full((N, K // 2), 0x22, np.uint8)    # packed fp4 weights: two codes for 1.0
     b_s = {"fp8_tensor": np.array([1.0], np.float32), "fp8_block128": np.ones((1, K // 128), np.float32),
            "mxfp8": np.full((N, K // 128), 127, np.uint8), "mxfp4": np.full((N, K // 32), 127, np.uint8),
-           "mxfp8_b32": np.full((N, K // 32), 127, np.uint8)}.get(mode)
+           "mxfp8_b32": np.full((N, K // 32), 127, np.uint8),
+           "mxfp4_fp8a": np.full((N, K // 32), 127, np.uint8)}.get(mode)
     c = Case(mode, A, B, _unit_a_scales(mode, M, K), b_s)
     for S in (1, 4):
         y = y_to_f64(c.gemm(split_k=S))
@@ -160,7 +183,7 @@ def test_all_ones_is_exact(mode):
 DECODE = [(m, n) for m, n in inputs.DECODE_SHAPES]
 
 
-@pytest.mark.parametrize("mode", ["fp8_tensor", "fp8_block128", "mxfp8", "mxfp4", "mxfp8_b32"])
+@pytest.mark.parametrize("mode", ["fp8_tensor", "fp8_block128", "mxfp8", "mxfp4", "mxfp8_b32", "mxfp4_fp8a"])
 @pytest.mark.parametrize("M,N", DECODE)
 def test_decode_workload_parity(mode, M, N):
     """The pages' decode shapes (K=7168) in the dispatch-chosen configuration,
@@ -235,7 +258,7 @@ def test_bounded_wait_reports_timeout_and_context_survives():
     FG_ERR_TIMEOUT.  A normal call afterwards is still correct."""
     M, N, K = 1, 256, 2048
     assert fg.get_error() == fg.FG_OK
-    for mode in ("fp8_tensor", "fp8_block128", "mxfp4"):
+    for mode in ("fp8_tensor", "fp8_block128", "mxfp4", "mxfp4_fp8a"):
         c = Case(mode, *inputs.operands(mode, M, N, K, 71, 72, 73))
         fg.set_wait_timeout_ns(20_000_000)
         try:

@@ -19,7 +19,7 @@ from tests.gpu_util import Case, y_to_f64
 pytestmark = pytest.mark.gpu
 
 
-@pytest.mark.parametrize("mode", ["bf16", "fp8_tensor", "mxfp8", "mxfp4", "mxfp8_b32"])
+@pytest.mark.parametrize("mode", ["bf16", "fp8_tensor", "mxfp8", "mxfp4", "mxfp8_b32", "mxfp4_fp8a"])
 @pytest.mark.parametrize("M,N,K", [(33, 256, 512), (129, 384, 1024), (300, 512, 2048), (1000, 1280, 1536)])
 def test_large_small_shapes(mode, M, N, K):
     c = Case(mode, *inputs.operands(mode, M, N, K, 10 + M, 20 + N, 30 + K))
@@ -28,7 +28,7 @@ def test_large_small_shapes(mode, M, N, K):
     parity.assert_y_close(y_to_f64(c.gemm()), c.ref(), f"{mode} {M}x{N}x{K}")
 
 
-@pytest.mark.parametrize("mode", ["bf16", "fp8_tensor", "mxfp8", "mxfp4", "mxfp8_b32"])
+@pytest.mark.parametrize("mode", ["bf16", "fp8_tensor", "mxfp8", "mxfp4", "mxfp8_b32", "mxfp4_fp8a"])
 def test_large_identity_is_bit_exact(mode):
     M, N, K = 300, 512, 1024
     _, B, _, b_s = inputs.operands(mode, 1, N, K, 3, 4, 5)
@@ -44,7 +44,7 @@ def test_large_identity_is_bit_exact(mode):
     elif mode == "mxfp4":
         A = inputs.pack_e2m1(A)
         a_s = np.full((M, K // 32), 127, np.uint8)
-    elif mode == "mxfp8_b32":
+    elif mode in ("mxfp8_b32", "mxfp4_fp8a"):
         a_s = np.full((M, K // 32), 127, np.uint8)
     c = Case(mode, A, B, a_s, b_s)
     ref = c.ref()
@@ -56,6 +56,7 @@ def test_large_identity_is_bit_exact(mode):
     ("bf16", 54560, 8192, 8192, "large_bf16_54560x8192x8192_fp8_4096x4096x8192", 0),
     ("mxfp8", 4096, 16384, 7168, "mx_mxfp8_mxfp4_n16384_k7168", 2),
     ("mxfp4", 4096, 16384, 7168, "mx_mxfp8_mxfp4_n16384_k7168", 5),
+    ("mxfp4_fp8a", 4096, 16384, 7168, "mx_fp8a_fp4w_n16384_k7168", 2),
 ])
 def test_large_workload_parity_sampled_rows(mode, M, N, K, name, idx):
     A, B, a_s, b_s = inputs.workload_operands(name, idx)

@@ -14,20 +14,22 @@ pytestmark = pytest.mark.gpu
 
 
 def _kb(mode, K):
-    return K * 2 if mode == "bf16" else (K // 2 if mode == "mxfp4" else K)
+    return K * 2 if mode == "bf16" else (K // 2 if mode in ("mxfp4", "mxfp4_fp8a") else K)
 
 
-@pytest.mark.parametrize("mode", ["bf16", "fp8_tensor", "fp8_block128", "mxfp8", "mxfp4", "mxfp8_b32"])
+@pytest.mark.parametrize("mode", ["bf16", "fp8_tensor", "fp8_block128", "mxfp8", "mxfp4", "mxfp8_b32", "mxfp4_fp8a"])
 @pytest.mark.parametrize("N,K", [(128, 256), (384, 1536), (256, 7168)])
 def test_relayout_matches_spec_and_inverts(mode, N, K):
     A, B, a_s, b_s = inputs.operands(mode, 1, N, K, 5, 6, 7)
     pb = fg.preshuffle_b(mode, dev(B), dev(b_s), K=K)
     torch.cuda.synchronize()
     kb = _kb(mode, K)
-    spec = oracle.preshuffle_b(np.ascontiguousarray(B).view(np.uint8).reshape(N, kb), N, kb)
+    Bb = np.ascontiguousarray(B).view(np.uint8).reshape(N, kb)
+    spec = oracle.block64_b(Bb, N, kb) if mode == "mxfp4_fp8a" else oracle.preshuffle_b(Bb, N, kb)
     assert np.array_equal(host(pb.data), spec)
-    if mode in ("mxfp8", "mxfp4", "mxfp8_b32"):
-        orc_mode = {"mxfp8": oracle.MXFP8, "mxfp4": oracle.MXFP4, "mxfp8_b32": oracle.MXFP8_B32}[mode]
+    if mode in ("mxfp8", "mxfp4", "mxfp8_b32", "mxfp4_fp8a"):
+        orc_mode = {"mxfp8": oracle.MXFP8, "mxfp4": oracle.MXFP4, "mxfp8_b32": oracle.MXFP8_B32,
+                    "mxfp4_fp8a": oracle.MXFP4_FP8A}[mode]
         assert np.array_equal(host(pb.sf), oracle.sf_image(orc_mode, b_s, N, K))
     back, sc = fg.unshuffle_b(pb)
     torch.cuda.synchronize()
