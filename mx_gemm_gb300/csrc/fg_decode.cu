@@ -8,7 +8,7 @@
 // in 16 TMEM columns.  CTA (nt, s, mt) covers weight rows [128 nt, +128),
 // token rows [16 mt, +16) and split s of the K slabs.
 //
-// Warp roles (192 threads):
+// Warp roles (192 threads; 320 for fp8 x fp4, see warps 6-9):
 //   warp 0    producer: one bulk copy per stage for the contiguous weight
 //             slabs of the preshuffled image, one TMA tensor load per slab
 //             for the token tile (rows beyond M are zero-filled), and for MX
@@ -30,6 +30,8 @@
 //             the same per-slab partials with a weight of 1: the fold is a
 //             compensated sum, which keeps the fp32 partials of long K
 //             splits within the workspace bound.
+//   warps 6-9 fp8 x fp4 only: expand half of every stage's packed fp4 weight
+//             blocks (the other half is done by warps 2-5), nothing else.
 //
 // Split-K reduction: with split > 1 the S split CTAs of a tile run as one
 // thread-block cluster, and CTA r owns rows [ceil(128 r/S), ceil(128 (r+1)/S))
@@ -87,6 +89,9 @@ struct DCfg {
   static constexpr int SFW_BYTES = SPS * APS * 512;
   static constexpr int SFT_BYTES = APS ? SPS * APS * 256 + 256 : 0;
   static constexpr int RAW_OFF = B_BYTES + A_BYTES + SFW_BYTES + SFT_BYTES;
+  // warps 2-5 (+ 6-9 when expanding): arrivals on a stage's full barrier
+  static constexpr int THREADS = EXPAND ? 320 : kThreads;
+  static constexpr int PREPASS_WARPS = EXPAND ? 8 : 4;
   static constexpr int RAW_BYTES = EXPAND ? SPS * 8192 : 0;
   static constexpr int STAGE_RAW = RAW_OFF + RAW_BYTES;
   static constexpr int STAGE_BYTES = (STAGE_RAW + 1023) / 1024 * 1024;
@@ -108,7 +113,7 @@ __device__ __forceinline__ uint32_t mx_idesc(int mode, int sfid) {
 }
 
 template <int MODE, int SPS, int STAGES>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(DCfg<MODE, SPS, STAGES>::THREADS, DCfg<MODE, SPS, STAGES>::EXPAND ? 2 : 1)
     decode_kernel(const __grid_constant__ CUtensorMap tmap_a, const DecodeParams p) {
   using C = DCfg<MODE, SPS, STAGES>;
   extern __shared__ uint8_t dsmem[];
@@ -139,7 +144,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < STAGES; ++i) {
-      mbar_init(&full_bar[i], C::APS ? 5 : 1);  // MX: + one arrival per scale-building warp
+      mbar_init(&full_bar[i], C::APS ? 1 + C::PREPASS_WARPS : 1);  // MX: + one arrival per pre-pass warp
       mbar_init(&empty_bar[i], 1);
       mbar_init(&raw_bar[i], 1);
     }
@@ -171,6 +176,28 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (p.fused_reduce) cluster_arrive_relaxed();
   const uint32_t tmem = tmem_base_sh;
   if (threadIdx.x == 0) pdl_launch_dependents();
+
+  // fp8 x fp4: expand the packed fp4 blocks of a stage (row r: 64 bytes, four
+  // 16-byte chunks of 32 codes) into the 128-byte-swizzled e4m3 tile: chunk
+  // c4 of row r becomes e4m3 chunks 2*c4 and 2*c4+1, stored at
+  // r*128 + ((c ^ (r%8))*16) like every other weight tile.  xt in [0, 256)
+  // picks this thread's two of each block's 512 chunks.
+  auto expand_stage = [&](int slot, int nsl, int xt) {
+    const uint8_t* raw = smem + slot * C::STAGE_BYTES + C::RAW_OFF;
+    uint8_t* tile = smem + slot * C::STAGE_BYTES;
+    for (int v = 0; v < nsl; ++v) {
+#pragma unroll
+      for (int q = 0; q < 2; ++q) {
+        const int c = q * 256 + xt;  // row c/4, quarter c%4
+        const int r = c >> 2, c4 = c & 3;
+        uint4 lo, hi;
+        e2m1x32_to_e4m3x32(*reinterpret_cast<const uint4*>(raw + v * 8192 + c * 16), lo, hi);
+        uint8_t* row = tile + v * kSlabBytes + r * 128;
+        *reinterpret_cast<uint4*>(row + (((2 * c4) ^ (r & 7)) << 4)) = lo;
+        *reinterpret_cast<uint4*>(row + (((2 * c4 + 1) ^ (r & 7)) << 4)) = hi;
+      }
+    }
+  };
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
@@ -337,6 +364,27 @@ __global__ void __launch_bounds__(kThreads, 1)
       cluster_wait();            // phase 1
       cluster_arrive_relaxed();  // phase 2 (this warp stores nothing into peers)
     }
+  } else if (C::EXPAND && warp >= 6) {
+    // ------------------------------------- fp4 expansion helpers (warps 6-9)
+    bool okx = true;
+    for (int it = 0; it < niter; ++it) {
+      const int slot = it % STAGES;
+      const bool w = mbar_wait(&empty_bar[slot], ((it / STAGES) & 1) ^ 1u, T, p.err, 13);
+      const bool wr = w && mbar_wait(&raw_bar[slot], (it / STAGES) & 1, T, p.err, 12);
+      if (!__all_sync(0xffffffffu, wr)) {
+        okx = false;
+        break;
+      }
+      expand_stage(slot, min(SPS, nslab - it * SPS), static_cast<int>(threadIdx.x) - 64);
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&full_bar[slot]);
+    }
+    if (!okx && lane == 0) abort_sh = 1;
+    if (p.fused_reduce) {
+      cluster_wait();            // phase 1
+      cluster_arrive_relaxed();  // phase 2 (these warps store nothing into peers)
+    }
   } else {
     // ------------------------------------------------------------ epilogue
     if (C::APS) {
@@ -385,29 +433,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (et < nsl * C::APS * kTokRows)
           *reinterpret_cast<uint32_t*>(sft + (et / kTokRows) * 256 + (et % kTokRows) * 16) = wv;
         if (C::EXPAND) {
-          // Expand the stage's packed fp4 weight blocks (row r: 64 bytes, four
-          // 16-byte chunks of 32 codes) into the 128-byte-swizzled e4m3 tile:
-          // chunk c4 of row r becomes e4m3 chunks 2*c4 and 2*c4+1, stored at
-          // r*128 + ((c ^ (r%8))*16) like every other weight tile.
           const bool wr = mbar_wait(&raw_bar[slot], (it / STAGES) & 1, T, p.err, 12);
           if (!__all_sync(0xffffffffu, wr)) {
             okb = false;
             break;
           }
-          const uint8_t* raw = smem + slot * C::STAGE_BYTES + C::RAW_OFF;
-          uint8_t* tile = smem + slot * C::STAGE_BYTES;
-          for (int v = 0; v < nsl; ++v) {
-#pragma unroll
-            for (int q = 0; q < 4; ++q) {
-              const int c = q * 128 + et;  // chunk of the block: row c/4, quarter c%4
-              const int r = c >> 2, c4 = c & 3;
-              uint4 lo, hi;
-              e2m1x32_to_e4m3x32(*reinterpret_cast<const uint4*>(raw + v * 8192 + c * 16), lo, hi);
-              uint8_t* row = tile + v * kSlabBytes + r * 128;
-              *reinterpret_cast<uint4*>(row + (((2 * c4) ^ (r & 7)) << 4)) = lo;
-              *reinterpret_cast<uint4*>(row + (((2 * c4 + 1) ^ (r & 7)) << 4)) = hi;
-            }
-          }
+          expand_stage(slot, nsl, et);
         }
         fence_proxy_async_smem();
         __syncwarp();
@@ -581,7 +612,7 @@ cudaError_t launch_one(const CUtensorMap& tmap_a, const DecodeParams& p, dim3 gr
   }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = grid;
-  cfg.blockDim = dim3(kThreads);
+  cfg.blockDim = dim3(C::THREADS);
   cfg.dynamicSmemBytes = C::SMEM;
   cfg.stream = stream;
   cudaLaunchAttribute attrs[2];
