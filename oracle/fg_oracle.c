@@ -27,8 +27,10 @@
  *                32 elements, next to the pages' 128-element "mx128")
  * and the same for B with n in place of m, except
  *   MXFP4_FP8A   Ad as MXFP8_B32, Bd as MXFP4: fp8 activations against fp4
- *                weights, both with one E8M0 per 32 K (the FlyDSL "MXFP4
- *                fp8-A" cases named in the split-K PR's test notes)
+ *                weights, both with one E8M0 per 32 K (the "MXFP4 fp8-A"
+ *                preshuffle-GEMM test cases named in the FlyDSL PR "Enable
+ *                the gmem->LDS async copy for f16/bf16 preshuffle GEMM",
+ *                Testing)
  *
  * Encodings are decoded from their bit fields through 256-entry tables built
  * once (OCP 8-bit floating point E4M3 "fn", OCP FP4 E2M1, E8M0, bfloat16).
