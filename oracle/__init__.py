@@ -192,10 +192,15 @@ def unblock64_b(img, N, Kb):
 
 
 def sf_image(mode, sf, N, K):
-    """MX weight-scale image (layout spec), uint8 of N/128 * slabs * atoms * 512 bytes."""
+    """MX weight-scale image (layout spec), uint8: N/128 * slabs * atoms * 512 bytes
+    (MXFP8: N/128 * ceil(slabs / 4) * 512, four 128-K slabs per atom)."""
     sf = _c(sf, np.uint8)
-    atoms, slab_k = (2, 256) if mode == MXFP4 else (1, 128)
-    out = np.zeros((N // 128) * (K // slab_k) * atoms * 512, np.uint8)
+    if mode == MXFP8:
+        n_atoms = (N // 128) * (-(-(K // 128) // 4))
+    else:
+        atoms, slab_k = (2, 256) if mode == MXFP4 else (1, 128)
+        n_atoms = (N // 128) * (K // slab_k) * atoms
+    out = np.zeros(n_atoms * 512, np.uint8)
     if lib().orc_sf_image(mode, _ptr(sf), N, K, _ptr(out)) != 0:
         raise ValueError("bad scale image arguments")
     return out

@@ -393,13 +393,17 @@ void orc_round_bf16(const double *in, int64_t n, uint16_t *out)
 /* ------------------------------------------- MX scale image (layout spec) */
 
 /*
- * The weight scale image of the MX modes.  For each 128-row tile nb, each
- * 128-byte K slab u and each atom a of the slab (one atom per slab for mxfp8,
- * two for mxfp4), a 512-byte atom whose byte 16*(r%32) + 4*(r/32) + j holds
- * the E8M0 scale of row nb*128 + r for the 32-K block (u*atoms + a)*4 + j.
- * An mxfp8 scale covers 128 K, i.e. the four 32-K blocks of its slab.
- * sf is [N][K/128] (mxfp8) or [N][K/32] (mxfp4, mxfp8 with 32-K blocks, and
- * the fp4 weights of MXFP4_FP8A, whose slab is 128 K like MXFP8_B32's).
+ * The weight scale image of the MX modes: 512-byte atoms whose byte
+ * 16*(r%32) + 4*(r/32) + j belongs to row nb*128 + r of 128-row tile nb.
+ *   MXFP4, MXFP8_B32 (and the fp4 weights of MXFP4_FP8A, whose slab is 128 K
+ *   like MXFP8_B32's): for each 128-byte K slab u and each atom a of the slab
+ *   (two per slab for MXFP4, one otherwise), byte j is the scale of the 32-K
+ *   block (u*atoms + a)*4 + j.  sf is [N][K/32].
+ *   MXFP8 (one scale per 128 K): for each group g of four consecutive slabs,
+ *   byte j is the scale of slab 4g + j (zero past the last slab).  sf is
+ *   [N][K/128].  (The layout is the implementation's own; packing four
+ *   slabs lets the kernels copy an atom into the tensor memory once per four
+ *   slabs, the MMA picking byte j by its scale-factor id.)
  */
 int orc_sf_image(int mode, const uint8_t *sf, int64_t N, int64_t K, uint8_t *out)
 {
@@ -407,19 +411,30 @@ int orc_sf_image(int mode, const uint8_t *sf, int64_t N, int64_t K, uint8_t *out
         mode = ORC_MXFP8_B32;
     if ((mode != ORC_MXFP8 && mode != ORC_MXFP4 && mode != ORC_MXFP8_B32) || N % 128 != 0)
         return -1;
+    if (mode == ORC_MXFP8) {
+        if (K % 128 != 0)
+            return -1;
+        const int64_t KB = K / 128, G = (KB + 3) / 4;
+        memset(out, 0, (size_t)((N / 128) * G * 512));
+        for (int64_t n = 0; n < N; ++n)
+            for (int64_t u = 0; u < KB; ++u) {
+                const int64_t nb = n / 128, r = n % 128;
+                out[(nb * G + u / 4) * 512 + 16 * (r % 32) + 4 * (r / 32) + u % 4] = sf[n * KB + u];
+            }
+        return 0;
+    }
     const int64_t slab_k = mode == ORC_MXFP4 ? 256 : 128;
     if (K % slab_k != 0)
         return -1;
     const int64_t atoms = mode == ORC_MXFP4 ? 2 : 1;
     const int64_t slabs = K / slab_k;
-    const int64_t cols = mode == ORC_MXFP8 ? K / 128 : K / 32;
+    const int64_t cols = K / 32;
     for (int64_t n = 0; n < N; ++n)
         for (int64_t q = 0; q < K / 32; ++q) {          /* 32-K block index */
             const int64_t nb = n / 128, r = n % 128;
             const int64_t u = q / (4 * atoms), a = (q / 4) % atoms, j = q % 4;
             const int64_t atom = (nb * slabs + u) * atoms + a;
-            const uint8_t v = mode == ORC_MXFP8 ? sf[n * cols + q / 4] : sf[n * cols + q];
-            out[atom * 512 + 16 * (r % 32) + 4 * (r / 32) + j] = v;
+            out[atom * 512 + 16 * (r % 32) + 4 * (r / 32) + j] = sf[n * cols + q];
         }
     return 0;
 }

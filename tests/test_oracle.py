@@ -454,10 +454,11 @@ def test_tolerance_check_catches_planted_mistakes():
 
 
 def test_sf_image_spec_is_a_bijection_onto_atoms():
-    """Every (row, 32-K block) scale lands in exactly one atom byte; the
-    128-K mxfp8 scale fills the four 32-K bytes of its slab."""
+    """Every scale lands in exactly one atom byte (one per 32-K block, or per
+    128-K slab for mxfp8, four slabs to an atom); the bytes a short last
+    mxfp8 group leaves over are zero."""
     for mode, cols_per_row, K in ((oracle.MXFP4, 7168 // 32, 7168), (oracle.MXFP8_B32, 1024 // 32, 1024),
-                                  (oracle.MXFP8, 1024 // 128, 1024)):
+                                  (oracle.MXFP8, 1024 // 128, 1024), (oracle.MXFP8, 640 // 128, 640)):
         N = 256
         ids = np.arange(N * cols_per_row, dtype=np.int64)
         for byte in range(2):   # unique 16-bit ids, one byte at a time
@@ -468,5 +469,12 @@ def test_sf_image_spec_is_a_bijection_onto_atoms():
             else:
                 hi = img.astype(np.int64)
         got = np.sort(lo | (hi << 8))
-        reps = 4 if mode == oracle.MXFP8 else 1
-        assert np.array_equal(got, np.sort(np.repeat(ids, reps)))
+        pad = got.size - ids.size
+        assert pad == ((N // 128) * 128 * (-cols_per_row % 4) if mode == oracle.MXFP8 else 0)
+        assert np.array_equal(got[pad:], np.sort(ids)) and not got[:pad].any()
+    # mxfp8: row r's scale for slab u sits at byte 16*(r%32) + 4*(r/32) + u%4 of atom (r/128, u/4)
+    N, K = 256, 896
+    sf = np.random.default_rng(9).integers(0, 255, (N, K // 128), dtype=np.uint8)
+    img = oracle.sf_image(oracle.MXFP8, sf, N, K).reshape(N // 128, 2, 512)
+    for r, u in ((0, 0), (37, 5), (200, 6), (255, 3)):
+        assert img[r // 128, u // 4, 16 * (r % 128 % 32) + 4 * (r % 128 // 32) + u % 4] == sf[r, u]
