@@ -119,7 +119,7 @@ uint64_t sf_image_bytes(int mode, int64_t N, int64_t K) {
   switch (mode) {
     case FG_FP8_TENSOR: return 16;
     case FG_FP8_BLOCK128: return static_cast<uint64_t>(N / 128) * (K / 128) * 4;
-    case FG_MXFP8:
+    case FG_MXFP8: return static_cast<uint64_t>(N / 128) * ((K / 128 + 3) / 4) * 512;  // four slabs per atom
     case FG_MXFP8_B32:
     case FG_MXFP4_FP8A: return static_cast<uint64_t>(N / 128) * (K / 128) * 512;
     case FG_MXFP4: return static_cast<uint64_t>(N / 128) * (K / 256) * 2 * 512;

@@ -229,10 +229,17 @@ __global__ void __launch_bounds__(DCfg<MODE, SPS, STAGES>::THREADS, DCfg<MODE, S
           bulk_g2s(st, p.b_img + (static_cast<size_t>(nt) * p.KB + u0 + ub) * kSlabBytes, nsl * kSlabBytes,
                    &full_bar[slot]);
         }
-        if (C::APS)
+        if (MODE == kMXFP8) {
+          // four slabs' scales to an atom: slab u's is byte u%4 of atom u/4
+          const int G = (p.KB + 3) / 4;
+          for (int v = 0; v < nsl; ++v)
+            bulk_g2s(st + C::B_BYTES + C::A_BYTES + v * 512,
+                     p.b_sf + (static_cast<size_t>(nt) * G + (u0 + ub + v) / 4) * 512, 512, &full_bar[slot]);
+        } else if (C::APS) {
           bulk_g2s(st + C::B_BYTES + C::A_BYTES,
                    p.b_sf + (static_cast<size_t>(nt) * p.KB + u0 + ub) * C::APS * 512, nsl * C::APS * 512,
                    &full_bar[slot]);
+        }
         if (it >= pre) {
           for (int v = 0; v < nsl; ++v)
             tma_load_2d(st + C::B_BYTES + v * kTokSlabBytes, &tmap_a, (u0 + ub + v) * 128, mt * kTokRows,
@@ -326,7 +333,12 @@ __global__ void __launch_bounds__(DCfg<MODE, SPS, STAGES>::THREADS, DCfg<MODE, S
               mma_f16(d, adesc, bdesc, idesc_bf16(128, kTokRows), acc);
             } else if (MODE == kTensor || MODE == kBlock) {
               mma_f8f6f4(d, adesc, bdesc, idesc_e4m3(128, kTokRows), acc);
-            } else if (MODE == kMXFP8 || MODE == kMXFP8B32 || MODE == kMXFP4FP8A) {
+            } else if (MODE == kMXFP8) {
+              // the weight's scale is byte (slab % 4) of its atom; the token
+              // atoms repeat theirs in all four bytes
+              mma_mxf8f6f4(d, adesc, bdesc, idesc_mx(128, kTokRows, 0u, (u0 + it * SPS + v) & 3, j),
+                           tmem + sfw_col + 4 * v, tmem + sft_col + 4 * v, acc);
+            } else if (MODE == kMXFP8B32 || MODE == kMXFP4FP8A) {
               mma_mxf8f6f4(d, adesc, bdesc, mx_idesc(MODE, j), tmem + sfw_col + 4 * v, tmem + sft_col + 4 * v, acc);
             } else {
               const int t = v * 2 + (j >> 1);

@@ -617,6 +617,11 @@ struct MxCfg {
   static constexpr int STAGE_BYTES = (STAGE_RAW + 1023) / 1024 * 1024;
   static constexpr int SMEM = kStages * STAGE_BYTES + 1024;
   static constexpr int SF_COLS = APS * 4 + APS * 8;  // TMEM columns per stage: A (128 rows) + B (256 rows)
+  // mxfp8: one atom holds four slabs' scales, so the scales are copied at
+  // the first slab of each group of four, into a ring of four group buffers
+  // (SF_COLS each) -- rewritten at least four slabs later, after the refill
+  // of that slab's stage has waited for the MMAs that read it
+  static constexpr bool GROUP4 = MODE == kMXFP8;
   static_assert(SMEM <= 232448, "shared memory budget");
   static_assert(256 + kStages * SF_COLS <= kTmemCols, "TMEM budget");
 };
@@ -677,15 +682,24 @@ __global__ void __launch_bounds__(kMxThreads, 1)
             break;
           }
           uint8_t* st = smem + slot * C::STAGE_BYTES;
-          mbar_arrive_expect_tx(&full_bar[slot], kABytes + C::SFA_BYTES + nslabs_n * (16384 + C::APS * 512));
+          const bool sf_here = !C::GROUP4 || (kb & 3) == 0;  // mxfp8: scales once per four slabs
+          const int G = (KB + 3) / 4;
+          mbar_arrive_expect_tx(&full_bar[slot], kABytes + nslabs_n * 16384 +
+                                                     (sf_here ? C::SFA_BYTES + nslabs_n * C::APS * 512 : 0));
           tma_load_2d(st, &tmap_a, kb * 128, tc.m * kBM, &full_bar[slot]);
-          bulk_g2s(st + kABytes + kBBytes, p.a_sf + (static_cast<size_t>(tc.m) * KB + kb) * C::SFA_BYTES,
-                   C::SFA_BYTES, &full_bar[slot]);
+          if (sf_here)
+            bulk_g2s(st + kABytes + kBBytes,
+                     p.a_sf + (C::GROUP4 ? static_cast<size_t>(tc.m) * G + kb / 4 : static_cast<size_t>(tc.m) * KB + kb) *
+                                  C::SFA_BYTES,
+                     C::SFA_BYTES, &full_bar[slot]);
           for (int h = 0; h < nslabs_n; ++h) {
             const size_t slab = static_cast<size_t>(2 * tc.n + h) * KB + kb;
             bulk_g2s(st + kABytes + h * 16384, p.b_img + slab * 16384, 16384, &full_bar[slot]);
-            bulk_g2s(st + kABytes + kBBytes + C::SFA_BYTES + h * C::APS * 512, p.b_sf + slab * C::APS * 512,
-                     C::APS * 512, &full_bar[slot]);
+            if (sf_here) {
+              const size_t atom = C::GROUP4 ? static_cast<size_t>(2 * tc.n + h) * G + kb / 4 : slab * C::APS;
+              bulk_g2s(st + kABytes + kBBytes + C::SFA_BYTES + h * C::APS * 512, p.b_sf + atom * 512, C::APS * 512,
+                       &full_bar[slot]);
+            }
           }
         }
       }
@@ -696,7 +710,7 @@ __global__ void __launch_bounds__(kMxThreads, 1)
     if (lane == 0) {
       bool ok = true;
       if (p.debug_stall) ok = mbar_wait(&stall_bar, 0, T, p.err, 22);
-      int it = 0, ti = 0;
+      int it = 0, ti = 0, gc = 0;  // gc: scale groups copied so far (mxfp8)
       for (int t = blockIdx.x; ok && t < tiles; t += gridDim.x, ++ti) {
         if (!mbar_wait(&acce_bar, (ti & 1) ^ 1u, T, p.err, 23)) {
           ok = false;
@@ -712,22 +726,29 @@ __global__ void __launch_bounds__(kMxThreads, 1)
           tc_fence_after();
           mma_any_sh = 1;
           uint8_t* st = smem + slot * C::STAGE_BYTES;
-          const uint32_t sfa = 256 + slot * C::SF_COLS;
+          const bool sf_here = !C::GROUP4 || (kb & 3) == 0;
+          if (C::GROUP4 && sf_here) ++gc;
+          const uint32_t sfa = 256 + (C::GROUP4 ? ((gc - 1) & 3) : slot) * C::SF_COLS;
           const uint32_t sfb = sfa + C::APS * 4;
           uint8_t* sfa_sm = st + kABytes + kBBytes;
           uint8_t* sfb_sm = sfa_sm + C::SFA_BYTES;
+          if (sf_here) {
 #pragma unroll
-          for (int g = 0; g < C::APS; ++g) {
-            tc_cp_32x128b_warpx4(tmem + sfa + 4 * g, sdesc_plain_rows16(smem_u32(sfa_sm + 512 * g)));
-            tc_cp_32x128b_warpx4(tmem + sfb + 8 * g, sdesc_plain_rows16(smem_u32(sfb_sm + 512 * g)));
-            tc_cp_32x128b_warpx4(tmem + sfb + 8 * g + 4,
-                                 sdesc_plain_rows16(smem_u32(sfb_sm + C::APS * 512 + 512 * g)));
+            for (int g = 0; g < C::APS; ++g) {
+              tc_cp_32x128b_warpx4(tmem + sfa + 4 * g, sdesc_plain_rows16(smem_u32(sfa_sm + 512 * g)));
+              tc_cp_32x128b_warpx4(tmem + sfb + 8 * g, sdesc_plain_rows16(smem_u32(sfb_sm + 512 * g)));
+              tc_cp_32x128b_warpx4(tmem + sfb + 8 * g + 4,
+                                   sdesc_plain_rows16(smem_u32(sfb_sm + C::APS * 512 + 512 * g)));
+            }
           }
 #pragma unroll
           for (int j = 0; j < 4; ++j) {
             const uint64_t adesc = sdesc_sw128(smem_u32(st + j * 32));
             const uint64_t bdesc = sdesc_sw128(smem_u32(st + kABytes + j * 32));
-            if (MODE == kMXFP8 || MODE == kMXFP8B32) {
+            if (MODE == kMXFP8) {  // byte kb % 4 of the group's atoms
+              mma_mxf8f6f4(tmem, adesc, bdesc, idesc_mx(kBM, kBN, 0u, kb & 3, kb & 3), tmem + sfa, tmem + sfb,
+                           (kb | j) != 0);
+            } else if (MODE == kMXFP8B32) {
               mma_mxf8f6f4(tmem, adesc, bdesc, idesc_mx(kBM, kBN, 0u, j, j), tmem + sfa, tmem + sfb, (kb | j) != 0);
             } else {
               const int g = j >> 1, id = 2 * (j & 1);

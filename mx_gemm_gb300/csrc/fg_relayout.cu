@@ -81,13 +81,30 @@ __global__ void expand_fp4_e4m3_kernel(const uint4* __restrict__ src, uint4* __r
   }
 }
 
-// MX weight scales [N][K/blk] (E8M0 bytes) <-> atoms of 512 bytes: for each
-// 128-row tile nb, slab u and atom a of the slab, byte 16*(r%32) + 4*(r/32) + j
-// holds the scale of row nb*128 + r for the 32-K block (u*APS + a)*4 + j.
-// mxfp8 scales cover 128 K, so the four 32-K blocks of a slab repeat one;
-// mxfp4 and the 32-block mxfp8 have one scale per 32-K block.
+// MX weight scales [N][K/blk] (E8M0 bytes) <-> atoms of 512 bytes whose byte
+// 16*(r%32) + 4*(r/32) + j belongs to row nb*128 + r.  mxfp4 and the 32-K
+// modes: for slab u and atom a of the slab, byte j is the scale of the 32-K
+// block (u*APS + a)*4 + j.  mxfp8 (one scale per 128-K slab): four slabs to
+// an atom, byte j the scale of slab 4g + j (zero past the last slab).
 __global__ void relayout_sf_kernel(const uint8_t* __restrict__ src, uint8_t* __restrict__ dst, int64_t N, int64_t K,
                                    int mode, int inverse) {
+  if (mode == kMXFP8) {
+    const int64_t KB = K / 128, G = (KB + 3) / 4;
+    const int64_t total = (N / 128) * G * 512;
+    for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < total;
+         i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+      const int64_t atom = i >> 9;
+      const int off = static_cast<int>(i & 511);
+      const int r = (off >> 4) + 32 * ((off & 15) >> 2);
+      const int64_t nb = atom / G, u = (atom - nb * G) * 4 + (off & 3);
+      const int64_t n = nb * 128 + r;
+      if (!inverse)
+        dst[i] = u < KB ? __ldg(src + n * KB + u) : uint8_t(0);
+      else if (u < KB)
+        dst[n * KB + u] = __ldg(src + i);
+    }
+    return;
+  }
   const int aps = mode == kMXFP4 ? 2 : 1;
   const int64_t KB = mode == kMXFP4 ? K / 256 : K / 128;  // slabs per row
   const int64_t sf_cols = mode == kMXFP8 ? K / 128 : K / 32;
@@ -112,10 +129,25 @@ __global__ void relayout_sf_kernel(const uint8_t* __restrict__ src, uint8_t* __r
 }
 
 // Activation scales of the MX modes, [rows][K/blk] E8M0 bytes, into the same
-// 512-byte atoms as the weight image, per 128-row tile of A; rows past the
-// end read as 2^0 (their A values are zero-filled by the tile loads).
+// 512-byte atoms as the weight image (mxfp8: four slabs to an atom), per
+// 128-row tile of A; rows past the end read as 2^0 (their A values are
+// zero-filled by the tile loads).
 __global__ void relayout_sf_rows_kernel(const uint8_t* __restrict__ src, uint8_t* __restrict__ dst, int64_t rows,
                                         int64_t K, int mode) {
+  if (mode == kMXFP8) {
+    const int64_t KB = K / 128, G = (KB + 3) / 4;
+    const int64_t total = ((rows + 127) / 128) * G * 512;
+    for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < total;
+         i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+      const int64_t atom = i >> 9;
+      const int off = static_cast<int>(i & 511);
+      const int r = (off >> 4) + 32 * ((off & 15) >> 2);
+      const int64_t mb = atom / G, u = (atom - mb * G) * 4 + (off & 3);
+      const int64_t m = mb * 128 + r;
+      dst[i] = u >= KB ? uint8_t(0) : (m < rows ? __ldg(src + m * KB + u) : uint8_t(127));
+    }
+    return;
+  }
   const int aps = mode == kMXFP4 ? 2 : 1;
   const int64_t KB = mode == kMXFP4 ? K / 256 : K / 128;
   const int64_t sf_cols = mode == kMXFP8 ? K / 128 : K / 32;
@@ -215,7 +247,7 @@ cudaError_t launch_relayout_sf(int mode, const uint8_t* src, uint8_t* dst, int64
                                cudaStream_t stream) {
   const int aps = mode == kMXFP4 ? 2 : 1;
   const int64_t KB = mode == kMXFP4 ? K / 256 : K / 128;
-  const int64_t work = (N / 128) * KB * aps * 512;
+  const int64_t work = mode == kMXFP8 ? (N / 128) * ((KB + 3) / 4) * 512 : (N / 128) * KB * aps * 512;
   if (work == 0) return cudaSuccess;
   relayout_sf_kernel<<<grid_for(work, 256), 256, 0, stream>>>(src, dst, N, K, mode, inverse ? 1 : 0);
   return cudaGetLastError();
@@ -224,6 +256,7 @@ cudaError_t launch_relayout_sf(int mode, const uint8_t* src, uint8_t* dst, int64
 uint64_t sf_rows_image_bytes(int mode, int64_t rows, int64_t K) {
   const int aps = mode == kMXFP4 ? 2 : 1;
   const int64_t KB = mode == kMXFP4 ? K / 256 : K / 128;
+  if (mode == kMXFP8) return static_cast<uint64_t>((rows + 127) / 128) * ((KB + 3) / 4) * 512;
   return static_cast<uint64_t>((rows + 127) / 128) * KB * aps * 512;
 }
 

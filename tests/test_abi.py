@@ -54,7 +54,8 @@ def test_version_and_status_names(fg):
     ("bf16", 256, 64, 256 * 128, 0),
     ("fp8_tensor", 2048, 7168, 2048 * 7168, 16),
     ("fp8_block128", 16384, 7168, 16384 * 7168, 128 * 56 * 4),
-    ("mxfp8", 16384, 7168, 16384 * 7168, 128 * 56 * 512),
+    ("mxfp8", 16384, 7168, 16384 * 7168, 128 * 14 * 512),
+    ("mxfp8", 256, 640, 256 * 640, 2 * 2 * 512),
     ("mxfp4", 16384, 7168, 16384 * 3584, 128 * 28 * 1024),
     ("mxfp8_b32", 16384, 7168, 16384 * 7168, 128 * 56 * 512),
     ("mxfp4_fp8a", 16384, 7168, 16384 * 3584, 128 * 56 * 512),
