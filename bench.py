@@ -63,6 +63,7 @@ WORKLOADS = {
                                              kind="large", idx=7, case_offset=2),
 }
 DEFAULT_WORKLOAD = "fp8_tensor_decode_sweep_k7168"
+MX_MODES = ("mxfp8", "mxfp4", "mxfp8_b32", "mxfp4_fp8a")
 
 
 def elem_bytes(mode, operand="a"):
@@ -191,7 +192,7 @@ class OracleSample:
             bs = b_s
             if c["mode"] == "fp8_block128":
                 bs = b_s[: (n + 127) // 128]
-            elif c["mode"] in ("mxfp8", "mxfp4", "mxfp8_b32", "mxfp4_fp8a"):
+            elif c["mode"] in MX_MODES:
                 bs = b_s[:n]
             self.oracle.gemm(self.orc[c["mode"]], A, B[:n], a_s, bs, M=c["M"], N=n, K=c["K"],
                              threads=self.threads)
@@ -566,11 +567,9 @@ def main():
     e2e_eager = whole_job_value(E, step_work, aggregate_ranks(e0.elapsed_time(e1), world, dist, dev), world,
                                 scale_u)
 
-    # + the per-call A scale relayout of the large MX form (and the weight
-    # expansion of fp8 x fp4)
+    # + the per-call A scale relayout of the large MX form
     launches_per_step = sum((2 if x["S"] > 8 else 1) +
-                            (1 if x["plan"]["path"] == 1 and x["c"]["mode"] in ("mxfp8", "mxfp4", "mxfp8_b32") else 0) +
-                            (2 if x["plan"]["path"] == 1 and x["c"]["mode"] == "mxfp4_fp8a" else 0)
+                            (1 if x["plan"]["path"] == 1 and x["c"]["mode"] in MX_MODES else 0)
                             for x in cases)
 
     cpu = None

@@ -106,8 +106,11 @@ typedef enum fg_mode {
  * tensor-core operand has in shared memory, so one pipeline stage of one
  * 128-row tile is one contiguous copy.  MXFP4_FP8A instead keeps the packed
  * fp4 bytes (Kb = K/2) in unswizzled blocks of 128 rows x 64 bytes (128 K),
- * block (nb, kb) at index nb*(K/128)+kb, row r at byte r*64: the kernels
- * expand each block to e4m3 (exactly: every e2m1 value is an e4m3 value).
+ * block (nb, kb) at index nb*(K/128)+kb, row r at byte r*64; the image must
+ * be 32-byte aligned.  The kernels load one block per tensor copy that puts
+ * every 16 codes in the low half of a 16-byte shared-memory chunk (the
+ * e2m1 operand form of the fp8/fp6/fp4 block-scaled MMA), so HBM moves
+ * only the packed bytes.
  *
  * Scale image (sf): FP8_TENSOR: the fp32 b_s (16 bytes reserved);
  * FP8_BLOCK128: b_s fp32 [N/128][K/128] unchanged; MXFP8 / MXFP8_B32 /
@@ -164,9 +167,10 @@ FG_API fg_status fg_preshuffle_b_size(int mode, int64_t N, int64_t K, uint64_t* 
  * One-time relayout of the weight B[N][K] (and of its scales) into the
  * images described above; fills *desc_out.  b_scales: FP8_TENSOR: device
  * fp32 scalar; FP8_BLOCK128: device fp32 [N/128][K/128]; MX: device uint8
- * E8M0 [N][K/128] (MXFP8) or [N][K/32] (MXFP4, MXFP8_B32); BF16: must be NULL.  B and the images must
+ * E8M0 [N][K/128] (MXFP8) or [N][K/32] (MXFP4, MXFP8_B32, MXFP4_FP8A); BF16: must be NULL.  B and the images must
  * not overlap.  Errors: INVALID_ARG, SHAPE, ALIGN (16 bytes for B and the
- * images, 4 for fp32 scales), WORKSPACE (an image buffer smaller than
+ * images -- 32 for the MXFP4_FP8A weight image --, 4 for fp32 scales),
+ * WORKSPACE (an image buffer smaller than
  * fg_preshuffle_b_size says), UNSUPPORTED_ARCH, CUDA.
  */
 FG_API fg_status fg_preshuffle_b(int mode, const void* B, const void* b_scales, int64_t N, int64_t K, void* b_image,

@@ -127,19 +127,8 @@ uint64_t sf_image_bytes(int mode, int64_t N, int64_t K) {
   }
 }
 
-// Workspace of the large-M MX kernel: A's scale atoms relaid per call and,
-// for MXFP4_FP8A, after them (256-byte aligned) the weights expanded to e4m3
-// (N*K bytes).  *expanded_at = that offset (0 when there is none).
-uint64_t large_mx_workspace(int mode, int64_t M, int64_t N, int64_t K, uint64_t* expanded_at) {
-  const uint64_t a_sf = sf_rows_image_bytes(mode, M, K);
-  if (mode != FG_MXFP4_FP8A) {
-    if (expanded_at) *expanded_at = 0;
-    return a_sf;
-  }
-  const uint64_t at = (a_sf + 255) / 256 * 256;
-  if (expanded_at) *expanded_at = at;
-  return at + static_cast<uint64_t>(N) * K;
-}
+// Workspace of the large-M MX kernel: A's scale atoms, relaid per call.
+uint64_t large_mx_workspace(int mode, int64_t M, int64_t K) { return sf_rows_image_bytes(mode, M, K); }
 
 // ------------------------------------------------------------ dispatch
 
@@ -327,6 +316,28 @@ fg_status make_tmap(CUtensorMap* map, const void* base, int64_t rows, int64_t rb
   return FG_OK;
 }
 
+// MXFP4_FP8A weight image (blocks of 128 rows x 64 bytes of packed e2m1, see
+// fg_preshuffle_b) as a 3-D map of 4-bit codes {128 codes, 128 rows,
+// N/128 * K/128 blocks}.  Its box is one block, loaded with every 16 codes
+// spread over 16 bytes of shared memory (codes in the low 8 bytes) in the
+// 128-byte swizzle: the e2m1 operand form of the mxf8f6f4 MMA.  The copy
+// counts the 8192 packed bytes of a block on its barrier.  The image must be
+// 32-byte aligned.
+fg_status make_tmap_fp4w(CUtensorMap* map, const void* base, int64_t N, int64_t K) {
+  auto fn = encode_fn();
+  if (!fn) return fail(FG_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
+  cuuint64_t dims[3] = {128, 128, static_cast<cuuint64_t>((N / 128) * (K / 128))};
+  cuuint64_t strides[2] = {64, 8192};
+  cuuint32_t box[3] = {128, 128, 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B, 3, const_cast<void*>(base), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS)
+    return fail(FG_ERR_CUDA, "cuTensorMapEncodeTiled (fp4 weight image) failed (%d)", static_cast<int>(r));
+  return FG_OK;
+}
+
 }  // namespace
 
 bool pdl_enabled() { return getenv("FG_NO_PDL") == nullptr; }
@@ -403,6 +414,8 @@ fg_status fg_preshuffle_b(int mode, const void* B, const void* b_scales, int64_t
   if (mode != FG_BF16 && (!b_scales || !sf_image)) return fail(FG_ERR_INVALID_ARG, "%s needs B scales and a scale image", mode_name(mode));
   if (!aligned(B, 16) || !aligned(b_image, 16) || (sf_image && !aligned(sf_image, 16)))
     return fail(FG_ERR_ALIGN, "B and the images must be 16-byte aligned");
+  if (mode == FG_MXFP4_FP8A && !aligned(b_image, 32))
+    return fail(FG_ERR_ALIGN, "the MXFP4_FP8A weight image must be 32-byte aligned");
   if (b_scales && !aligned(b_scales, is_mx(mode) ? 1 : 4))
     return fail(FG_ERR_ALIGN, "fp32 scales must be 4-byte aligned");
   if (b_image_bytes < need_b || sf_image_bytes < need_sf)
@@ -486,7 +499,7 @@ fg_status fg_gemm_workspace_size(int mode, int64_t M, int64_t N, int64_t K, int 
   if (s != FG_OK) return s;
   if (plan.path == 1) {
     const int64_t tiles = ((M + plan.tile_m - 1) / plan.tile_m) * (N / 256 + (N % 256 ? 1 : 0));
-    *bytes = is_mx(mode) ? large_mx_workspace(mode, M, N, K, nullptr)
+    *bytes = is_mx(mode) ? large_mx_workspace(mode, M, K)
                          : large_streamk_plan(mode, tiles, row_bytes(mode, K) / 128, plan.ctas, nullptr,
                                               plan.tile_m == 256);
   }
@@ -530,11 +543,10 @@ fg_status fg_gemm(const void* A, const void* a_scales, int64_t M, const fg_bshuf
   }
   if (plan.path == 1 && mx) {
     // the large-M MX kernel reads A's scales as 512-byte atoms relaid per call
-    // (and MXFP4_FP8A's weights expanded to e4m3)
-    const uint64_t need = large_mx_workspace(mode, M, N, K, nullptr);
+    const uint64_t need = large_mx_workspace(mode, M, K);
     if (!workspace || workspace_bytes < need)
-      return fail(FG_ERR_WORKSPACE, "large-M %s needs a %llu-byte workspace for the A scale image%s", mode_name(mode),
-                  (unsigned long long)need, mode == FG_MXFP4_FP8A ? " and the expanded weights" : "");
+      return fail(FG_ERR_WORKSPACE, "large-M %s needs a %llu-byte workspace for the A scale image", mode_name(mode),
+                  (unsigned long long)need);
     if (!aligned(workspace, 16)) return fail(FG_ERR_ALIGN, "workspace must be 16-byte aligned");
   }
   if ((s = check_arch()) != FG_OK) return s;
@@ -543,6 +555,9 @@ fg_status fg_gemm(const void* A, const void* a_scales, int64_t M, const fg_bshuf
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   const int64_t rb = row_bytes(mode, K);
   CUtensorMap tmap;
+  CUtensorMap tmap_b;
+  memset(&tmap_b, 0, sizeof tmap_b);
+  if (mode == FG_MXFP4_FP8A && (s = make_tmap_fp4w(&tmap_b, b->data, N, K)) != FG_OK) return s;
   cudaError_t e;
   if (plan.path == 1) {
     if ((s = make_tmap(&tmap, A, M, rb, 128)) != FG_OK) return s;
@@ -576,25 +591,13 @@ fg_status fg_gemm(const void* A, const void* a_scales, int64_t M, const fg_bshuf
         large_streamk_plan(mode, 0, 0, 0, &p, false);  // all tiles whole
       }
     }
-    int kernel_mode = mode;
     if (mx) {
       e = launch_relayout_sf_rows(mode, static_cast<const uint8_t*>(a_scales), static_cast<uint8_t*>(workspace), M, K,
                                   st);
       if (e != cudaSuccess) return cuda_fail(e, "A scale relayout launch");
       p.a_sf = static_cast<const uint8_t*>(workspace);
     }
-    if (mode == FG_MXFP4_FP8A) {
-      // the fp4 weights expanded once per call to the e4m3 image of the same
-      // values; from there on this is the e4m3 x e4m3 32-K-block GEMM
-      uint64_t at = 0;
-      large_mx_workspace(mode, M, N, K, &at);
-      uint8_t* expanded = static_cast<uint8_t*>(workspace) + at;
-      e = launch_expand_fp4_e4m3(static_cast<const uint8_t*>(b->data), expanded, N, K, st);
-      if (e != cudaSuccess) return cuda_fail(e, "weight expansion launch");
-      p.b_img = expanded;
-      kernel_mode = kMXFP8B32;
-    }
-    e = launch_large(kernel_mode, tmap, p, plan.ctas, st);
+    e = launch_large(mode, tmap, tmap_b, p, plan.ctas, st);
     if (e != cudaSuccess) return cuda_fail(e, "large-M kernel launch");
     return FG_OK;
   }
@@ -620,7 +623,7 @@ fg_status fg_gemm(const void* A, const void* a_scales, int64_t M, const fg_bshuf
   if (!decode_config_supported(cfg)) return fail(FG_ERR_INVALID_ARG, "no kernel for config %s", plan.name);
   dim3 grid(static_cast<unsigned>(N / 128), static_cast<unsigned>(split), static_cast<unsigned>((M + 15) / 16));
   if (grid.z > 65535) return fail(FG_ERR_SHAPE, "M=%lld too large for the decode path", (long long)M);
-  e = launch_decode(cfg, tmap, p, grid, st);
+  e = launch_decode(cfg, tmap, tmap_b, p, grid, st);
   if (e != cudaSuccess) return cuda_fail(e, "decode kernel launch");
   if (split > 1 && !defer && !fused) {
     const float* as = mode == FG_FP8_TENSOR ? static_cast<const float*>(a_scales) : nullptr;

@@ -8,18 +8,22 @@
 // in 16 TMEM columns.  CTA (nt, s, mt) covers weight rows [128 nt, +128),
 // token rows [16 mt, +16) and split s of the K slabs.
 //
-// Warp roles (192 threads; 320 for fp8 x fp4, see warps 6-9):
+// Warp roles (192 threads):
 //   warp 0    producer: one bulk copy per stage for the contiguous weight
 //             slabs of the preshuffled image, one TMA tensor load per slab
 //             for the token tile (rows beyond M are zero-filled), and for MX
-//             the weight scale atoms (bulk);
+//             the weight scale atoms (bulk).  fp4 weights against fp8
+//             activations come as packed blocks (128 rows x 64 bytes) through
+//             a tensor load that spreads every 16 codes over a 16-byte
+//             shared-memory chunk (codes in its low 8 bytes), 128-byte
+//             swizzled: the sub-byte operand form of the fp8/fp6/fp4 MMA, so
+//             the MMA reads fp4 straight from the copy while HBM moves only
+//             the packed bytes;
 //   warp 1    allocates TMEM; lane 0 issues tcgen05.cp (MX scale factors)
 //             and tcgen05.mma, and commits stage releases;
 //   warps 2-5 for MX, first build the token scale atoms of each stage from
 //             the caller's E8M0 bytes (ahead of the MMA, one arrival per warp
-//             on the stage's full barrier) -- for fp8 activations against
-//             fp4 weights they also expand the stage's packed fp4 weight
-//             blocks into the e4m3 tile the MMA reads; then
+//             on the stage's full barrier); then
 //             epilogue: TMEM -> registers -> fp32 partials (split > 1) or
 //             scaled bf16 Y (split == 1).  For FP8_BLOCK128 they also run
 //             the per-128-K promotion: each K slab (one 128-K scale block)
@@ -30,8 +34,6 @@
 //             the same per-slab partials with a weight of 1: the fold is a
 //             compensated sum, which keeps the fp32 partials of long K
 //             splits within the workspace bound.
-//   warps 6-9 fp8 x fp4 only: expand half of every stage's packed fp4 weight
-//             blocks (the other half is done by warps 2-5), nothing else.
 //
 // Split-K reduction: with split > 1 the S split CTAs of a tile run as one
 // thread-block cluster, and CTA r owns rows [ceil(128 r/S), ceil(128 (r+1)/S))
@@ -77,23 +79,22 @@ constexpr int kThreads = 192;
 constexpr int kSlabBytes = 16384;   // 128 rows x 128 bytes
 constexpr int kTokSlabBytes = 2048; // 16 rows x 128 bytes
 constexpr int kTokRows = 16;
+// fp4 weight block of one slab: 128 rows x 64 packed bytes.  Its tensor load
+// writes kSlabBytes of shared memory and counts these bytes on the barrier.
+constexpr int kFp4SlabBytes = 8192;
 
 template <int MODE, int SPS, int STAGES>
 struct DCfg {
   static constexpr int APS = MODE == kMXFP4 ? 2 : (is_mx(MODE) ? 1 : 0);
-  // fp8 activations x fp4 weights: the weight arrives as packed fp4 blocks
-  // (128 rows x 64 bytes per slab) in a staging area and is expanded to e4m3
-  static constexpr bool EXPAND = MODE == kMXFP4FP8A;
+  // fp8 activations x fp4 weights: packed fp4 blocks through the spreading
+  // tensor load (a 16 KiB tile per slab in shared memory, 8 KiB from HBM)
+  static constexpr bool FP4W = MODE == kMXFP4FP8A;
   static constexpr int B_BYTES = SPS * kSlabBytes;
   static constexpr int A_BYTES = SPS * kTokSlabBytes;
   static constexpr int SFW_BYTES = SPS * APS * 512;
   static constexpr int SFT_BYTES = APS ? SPS * APS * 256 + 256 : 0;
-  static constexpr int RAW_OFF = B_BYTES + A_BYTES + SFW_BYTES + SFT_BYTES;
-  // warps 2-5 (+ 6-9 when expanding): arrivals on a stage's full barrier
-  static constexpr int THREADS = EXPAND ? 320 : kThreads;
-  static constexpr int PREPASS_WARPS = EXPAND ? 8 : 4;
-  static constexpr int RAW_BYTES = EXPAND ? SPS * 8192 : 0;
-  static constexpr int STAGE_RAW = RAW_OFF + RAW_BYTES;
+  static constexpr int PREPASS_WARPS = 4;  // warps 2-5: arrivals on an MX stage's full barrier
+  static constexpr int STAGE_RAW = B_BYTES + A_BYTES + SFW_BYTES + SFT_BYTES;
   static constexpr int STAGE_BYTES = (STAGE_RAW + 1023) / 1024 * 1024;
   static constexpr int NBUF = 8;  // blockscale TMEM partial buffers
   static constexpr int SF_COLS = SPS * APS * 4;  // TMEM columns per operand per stage
@@ -108,13 +109,19 @@ struct DCfg {
   static_assert(SMEM <= 232448, "shared memory budget");
 };
 
+// The weight is the MMA's A operand, the tokens its B operand.
 __device__ __forceinline__ uint32_t mx_idesc(int mode, int sfid) {
-  return mode == kMXFP4 ? idesc_mx(128, kTokRows, 1u, sfid, sfid) : idesc_mx(128, kTokRows, 0u, sfid, sfid);
+  return mode == kMXFP4        ? idesc_mx(128, kTokRows, kMxf4E2M1, sfid, sfid)
+         : mode == kMXFP4FP8A ? idesc_mx_ab(128, kTokRows, kF8f6f4E2M1, kF8f6f4E4M3, sfid, sfid)
+                               : idesc_mx(128, kTokRows, kF8f6f4E4M3, sfid, sfid);
 }
 
+// tmap_b: fp8 x fp4 only, the weight image as [blocks][128 rows][128 codes]
+// (see the producer); unused otherwise.
 template <int MODE, int SPS, int STAGES>
-__global__ void __launch_bounds__(DCfg<MODE, SPS, STAGES>::THREADS, DCfg<MODE, SPS, STAGES>::EXPAND ? 2 : 1)
-    decode_kernel(const __grid_constant__ CUtensorMap tmap_a, const DecodeParams p) {
+__global__ void __launch_bounds__(kThreads, 1)
+    decode_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_b,
+                  const DecodeParams p) {
   using C = DCfg<MODE, SPS, STAGES>;
   extern __shared__ uint8_t dsmem[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(dsmem) + 1023) & ~uintptr_t(1023));
@@ -125,7 +132,6 @@ __global__ void __launch_bounds__(DCfg<MODE, SPS, STAGES>::THREADS, DCfg<MODE, S
   __shared__ __align__(8) uint64_t pempty_bar[C::NBUF];
   __shared__ __align__(8) uint64_t acc_bar, stall_bar, drain_bar;
   __shared__ __align__(8) uint64_t ready_bar, recv_bar;  // fused split-K reduce
-  __shared__ __align__(8) uint64_t raw_bar[STAGES];      // packed fp4 weights landed (EXPAND)
   __shared__ uint32_t tmem_base_sh;
   __shared__ int abort_sh, issued_sh, consumed_sh, mma_any_sh;
 
@@ -146,7 +152,6 @@ __global__ void __launch_bounds__(DCfg<MODE, SPS, STAGES>::THREADS, DCfg<MODE, S
     for (int i = 0; i < STAGES; ++i) {
       mbar_init(&full_bar[i], C::APS ? 1 + C::PREPASS_WARPS : 1);  // MX: + one arrival per pre-pass warp
       mbar_init(&empty_bar[i], 1);
-      mbar_init(&raw_bar[i], 1);
     }
     for (int i = 0; i < C::NBUF; ++i) {
       mbar_init(&pfull_bar[i], 1);
@@ -167,7 +172,10 @@ __global__ void __launch_bounds__(DCfg<MODE, SPS, STAGES>::THREADS, DCfg<MODE, S
     tmem_alloc(&tmem_base_sh, C::TMEM_COLS);
     tmem_relinquish();
   }
-  if (warp == 0 && lane == 0) prefetch_tmap(&tmap_a);
+  if (warp == 0 && lane == 0) {
+    prefetch_tmap(&tmap_a);
+    if (C::FP4W) prefetch_tmap(&tmap_b);
+  }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -176,28 +184,6 @@ __global__ void __launch_bounds__(DCfg<MODE, SPS, STAGES>::THREADS, DCfg<MODE, S
   if (p.fused_reduce) cluster_arrive_relaxed();
   const uint32_t tmem = tmem_base_sh;
   if (threadIdx.x == 0) pdl_launch_dependents();
-
-  // fp8 x fp4: expand the packed fp4 blocks of a stage (row r: 64 bytes, four
-  // 16-byte chunks of 32 codes) into the 128-byte-swizzled e4m3 tile: chunk
-  // c4 of row r becomes e4m3 chunks 2*c4 and 2*c4+1, stored at
-  // r*128 + ((c ^ (r%8))*16) like every other weight tile.  xt in [0, 256)
-  // picks this thread's two of each block's 512 chunks.
-  auto expand_stage = [&](int slot, int nsl, int xt) {
-    const uint8_t* raw = smem + slot * C::STAGE_BYTES + C::RAW_OFF;
-    uint8_t* tile = smem + slot * C::STAGE_BYTES;
-    for (int v = 0; v < nsl; ++v) {
-#pragma unroll
-      for (int q = 0; q < 2; ++q) {
-        const int c = q * 256 + xt;  // row c/4, quarter c%4
-        const int r = c >> 2, c4 = c & 3;
-        uint4 lo, hi;
-        e2m1x32_to_e4m3x32(*reinterpret_cast<const uint4*>(raw + v * 8192 + c * 16), lo, hi);
-        uint8_t* row = tile + v * kSlabBytes + r * 128;
-        *reinterpret_cast<uint4*>(row + (((2 * c4) ^ (r & 7)) << 4)) = lo;
-        *reinterpret_cast<uint4*>(row + (((2 * c4 + 1) ^ (r & 7)) << 4)) = hi;
-      }
-    }
-  };
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
@@ -218,12 +204,11 @@ __global__ void __launch_bounds__(DCfg<MODE, SPS, STAGES>::THREADS, DCfg<MODE, S
       const int nsl = min(SPS, nslab - ub);
       uint8_t* st = smem + slot * C::STAGE_BYTES;
       if (lane == 0) {
-        if (C::EXPAND) {
-          // packed fp4 blocks into the staging area, on their own barrier
-          mbar_arrive_expect_tx(&raw_bar[slot], nsl * 8192);
-          bulk_g2s(st + C::RAW_OFF, p.b_img + (static_cast<size_t>(nt) * p.KB + u0 + ub) * 8192, nsl * 8192,
-                   &raw_bar[slot]);
-          mbar_arrive_expect_tx(&full_bar[slot], nsl * (kTokSlabBytes + C::APS * 512));
+        if (C::FP4W) {
+          // block (nt, u) of the image is z = nt * KB + u of the tensor map
+          mbar_arrive_expect_tx(&full_bar[slot], nsl * (kFp4SlabBytes + kTokSlabBytes + C::APS * 512));
+          for (int v = 0; v < nsl; ++v)
+            tma_load_3d(st + v * kSlabBytes, &tmap_b, 0, 0, nt * p.KB + u0 + ub + v, &full_bar[slot]);
         } else {
           mbar_arrive_expect_tx(&full_bar[slot], nsl * (kSlabBytes + kTokSlabBytes + C::APS * 512));
           bulk_g2s(st, p.b_img + (static_cast<size_t>(nt) * p.KB + u0 + ub) * kSlabBytes, nsl * kSlabBytes,
@@ -376,27 +361,6 @@ __global__ void __launch_bounds__(DCfg<MODE, SPS, STAGES>::THREADS, DCfg<MODE, S
       cluster_wait();            // phase 1
       cluster_arrive_relaxed();  // phase 2 (this warp stores nothing into peers)
     }
-  } else if (C::EXPAND && warp >= 6) {
-    // ------------------------------------- fp4 expansion helpers (warps 6-9)
-    bool okx = true;
-    for (int it = 0; it < niter; ++it) {
-      const int slot = it % STAGES;
-      const bool w = mbar_wait(&empty_bar[slot], ((it / STAGES) & 1) ^ 1u, T, p.err, 13);
-      const bool wr = w && mbar_wait(&raw_bar[slot], (it / STAGES) & 1, T, p.err, 12);
-      if (!__all_sync(0xffffffffu, wr)) {
-        okx = false;
-        break;
-      }
-      expand_stage(slot, min(SPS, nslab - it * SPS), static_cast<int>(threadIdx.x) - 64);
-      fence_proxy_async_smem();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&full_bar[slot]);
-    }
-    if (!okx && lane == 0) abort_sh = 1;
-    if (p.fused_reduce) {
-      cluster_wait();            // phase 1
-      cluster_arrive_relaxed();  // phase 2 (these warps store nothing into peers)
-    }
   } else {
     // ------------------------------------------------------------ epilogue
     if (C::APS) {
@@ -444,14 +408,6 @@ __global__ void __launch_bounds__(DCfg<MODE, SPS, STAGES>::THREADS, DCfg<MODE, S
         uint8_t* sft = smem + slot * C::STAGE_BYTES + C::B_BYTES + C::A_BYTES + C::SFW_BYTES;
         if (et < nsl * C::APS * kTokRows)
           *reinterpret_cast<uint32_t*>(sft + (et / kTokRows) * 256 + (et % kTokRows) * 16) = wv;
-        if (C::EXPAND) {
-          const bool wr = mbar_wait(&raw_bar[slot], (it / STAGES) & 1, T, p.err, 12);
-          if (!__all_sync(0xffffffffu, wr)) {
-            okb = false;
-            break;
-          }
-          expand_stage(slot, nsl, et);
-        }
         fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) mbar_arrive(&full_bar[slot]);
@@ -601,7 +557,6 @@ __global__ void __launch_bounds__(DCfg<MODE, SPS, STAGES>::THREADS, DCfg<MODE, S
     // away, and every MMA it issued finish before TMEM is released.
     if (threadIdx.x == 0) {
       for (int it = consumed_sh; it < issued_sh; ++it) {
-        if (C::EXPAND) mbar_wait(&raw_bar[it % STAGES], (it / STAGES) & 1, T, nullptr, 0);
         mbar_wait(&full_bar[it % STAGES], (it / STAGES) & 1, T, nullptr, 0);
       }
     }
@@ -613,7 +568,8 @@ __global__ void __launch_bounds__(DCfg<MODE, SPS, STAGES>::THREADS, DCfg<MODE, S
 }
 
 template <int MODE, int SPS, int STAGES>
-cudaError_t launch_one(const CUtensorMap& tmap_a, const DecodeParams& p, dim3 grid, cudaStream_t stream) {
+cudaError_t launch_one(const CUtensorMap& tmap_a, const CUtensorMap& tmap_b, const DecodeParams& p, dim3 grid,
+                       cudaStream_t stream) {
   using C = DCfg<MODE, SPS, STAGES>;
   static bool attr_set = false;  // per process; the attribute applies to every device
   if (!attr_set) {
@@ -624,7 +580,7 @@ cudaError_t launch_one(const CUtensorMap& tmap_a, const DecodeParams& p, dim3 gr
   }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = grid;
-  cfg.blockDim = dim3(C::THREADS);
+  cfg.blockDim = dim3(kThreads);
   cfg.dynamicSmemBytes = C::SMEM;
   cfg.stream = stream;
   cudaLaunchAttribute attrs[2];
@@ -643,7 +599,7 @@ cudaError_t launch_one(const CUtensorMap& tmap_a, const DecodeParams& p, dim3 gr
   }
   cfg.attrs = attrs;
   cfg.numAttrs = na;
-  return cudaLaunchKernelEx(&cfg, decode_kernel<MODE, SPS, STAGES>, tmap_a, p);
+  return cudaLaunchKernelEx(&cfg, decode_kernel<MODE, SPS, STAGES>, tmap_a, tmap_b, p);
 }
 
 // Instantiated configurations: (slabs per stage, stages).
@@ -655,35 +611,27 @@ cudaError_t launch_one(const CUtensorMap& tmap_a, const DecodeParams& p, dim3 gr
   X(MODE, 2, 3)                    \
   X(MODE, 2, 5)                    \
   X(MODE, 4, 2)
-#define FG_DECODE_CONFIGS_EXPAND(X, MODE) \
-  X(MODE, 1, 4)                           \
-  X(MODE, 1, 5)                           \
-  X(MODE, 1, 6)                           \
-  X(MODE, 1, 8)                           \
-  X(MODE, 2, 3)                           \
-  X(MODE, 4, 2)
 
 }  // namespace
 
 bool decode_config_supported(const DecodeConfig& c) {
   if (c.mode < kBF16 || c.mode > kMXFP4FP8A) return false;
-  // with its fp4 staging area, 2 slabs x 5 stages exceed shared memory
-  if (c.mode == kMXFP4FP8A && c.sps == 2 && c.stages == 5) return false;
   return (c.sps == 1 && (c.stages == 4 || c.stages == 5 || c.stages == 6 || c.stages == 8)) ||
          (c.sps == 2 && (c.stages == 3 || c.stages == 5)) || (c.sps == 4 && c.stages == 2);
 }
 
-cudaError_t launch_decode(const DecodeConfig& c, const CUtensorMap& tmap_a, const DecodeParams& p, dim3 grid,
-                          cudaStream_t stream) {
-#define FG_TRY(MODE_, SPS_, ST_) \
-  if (c.mode == MODE_ && c.sps == SPS_ && c.stages == ST_) return launch_one<MODE_, SPS_, ST_>(tmap_a, p, grid, stream);
+cudaError_t launch_decode(const DecodeConfig& c, const CUtensorMap& tmap_a, const CUtensorMap& tmap_b,
+                          const DecodeParams& p, dim3 grid, cudaStream_t stream) {
+#define FG_TRY(MODE_, SPS_, ST_)                                 \
+  if (c.mode == MODE_ && c.sps == SPS_ && c.stages == ST_)       \
+    return launch_one<MODE_, SPS_, ST_>(tmap_a, tmap_b, p, grid, stream);
   FG_DECODE_CONFIGS(FG_TRY, kBF16)
   FG_DECODE_CONFIGS(FG_TRY, kTensor)
   FG_DECODE_CONFIGS(FG_TRY, kBlock)
   FG_DECODE_CONFIGS(FG_TRY, kMXFP8)
   FG_DECODE_CONFIGS(FG_TRY, kMXFP4)
   FG_DECODE_CONFIGS(FG_TRY, kMXFP8B32)
-  FG_DECODE_CONFIGS_EXPAND(FG_TRY, kMXFP4FP8A)
+  FG_DECODE_CONFIGS(FG_TRY, kMXFP4FP8A)
 #undef FG_TRY
   return cudaErrorInvalidValue;
 }

@@ -82,12 +82,16 @@ uint64_t large_streamk_bytes(int ctas, bool wide);
 bool decode_config_supported(const DecodeConfig& c);
 // Kernels are launched with programmatic dependent launch (they may start
 // while the previous kernel of the stream finishes; they wait for it before
-// touching anything it could write or read).
-cudaError_t launch_decode(const DecodeConfig& cfg, const CUtensorMap& tmap_a, const DecodeParams& p, dim3 grid,
-                          cudaStream_t stream);
+// touching anything it could write or read).  tmap_b: kMXFP4FP8A's weight
+// image as a 3-D map of 4-bit codes {128 codes, 128 rows, N/128 * K/128
+// blocks}, loaded one block at a time with each 16 codes spread over 16
+// bytes of shared memory (unused by the other modes).
+cudaError_t launch_decode(const DecodeConfig& cfg, const CUtensorMap& tmap_a, const CUtensorMap& tmap_b,
+                          const DecodeParams& p, dim3 grid, cudaStream_t stream);
 
 bool large_supported(int mode);
-cudaError_t launch_large(int mode, const CUtensorMap& tmap_a, const LargeParams& p, int ctas, cudaStream_t stream);
+cudaError_t launch_large(int mode, const CUtensorMap& tmap_a, const CUtensorMap& tmap_b, const LargeParams& p,
+                         int ctas, cudaStream_t stream);
 
 cudaError_t launch_relayout_b(const uint8_t* src, uint8_t* dst, int64_t N, int64_t Kb, bool inverse,
                               cudaStream_t stream);
@@ -96,9 +100,6 @@ cudaError_t launch_relayout_sf(int mode, const uint8_t* src, uint8_t* dst, int64
 // kMXFP4FP8A weight image: packed fp4 [N][Kb] <-> 128-row x 64-byte blocks.
 cudaError_t launch_block64_b(const uint8_t* src, uint8_t* dst, int64_t N, int64_t Kb, bool inverse,
                              cudaStream_t stream);
-// kMXFP4FP8A weight image -> the e4m3 weight image (128-byte-swizzled slabs)
-// of the same values, N*K bytes.
-cudaError_t launch_expand_fp4_e4m3(const uint8_t* src, uint8_t* dst, int64_t N, int64_t K, cudaStream_t stream);
 uint64_t sf_rows_image_bytes(int mode, int64_t rows, int64_t K);
 cudaError_t launch_relayout_sf_rows(int mode, const uint8_t* src, uint8_t* dst, int64_t rows, int64_t K,
                                     cudaStream_t stream);

@@ -599,10 +599,14 @@ cudaError_t launch_wide(const CUtensorMap& tmap_a, const LargeParams& p, int cta
 //
 // Block-scaled variant (mxfp8: kind::mxf8f6f4, one E8M0 per 32 K of the
 // hardware block -- the 128-K mxfp8 scale repeated four times in the atoms;
-// mxfp4: kind::mxf4 with two E8M0 per 64-K MMA).  Per stage the producer
-// also bulk-copies the scale atoms of the A tile (from the per-call A scale
-// image) and of the two weight slabs; the MMA thread moves them into a TMEM
-// ring with tcgen05.cp before the stage's MMAs.  TMEM holds one 256-column
+// mxfp4: kind::mxf4 with two E8M0 per 64-K MMA; fp8 activations against fp4
+// weights: kind::mxf8f6f4 with an e4m3 A and an e2m1 B, the weight blocks
+// loaded by a tensor copy that spreads every 16 packed codes over a 16-byte
+// shared-memory chunk -- the sub-byte operand form this kind reads -- so the
+// weight tile has the geometry of an e4m3 tile and HBM moves the packed
+// bytes).  Per stage the producer also bulk-copies the scale atoms of the A
+// tile (from the per-call A scale image) and of the two weight slabs; the MMA
+// thread moves them into a TMEM ring with tcgen05.cp before the stage's MMAs.  TMEM holds one 256-column
 // accumulator plus that ring, so the epilogue runs on eight warps that each
 // pull their 128 columns into registers and release the accumulator before
 // converting and storing -- the next tile's MMAs overlap the stores.
@@ -626,9 +630,12 @@ struct MxCfg {
   static_assert(256 + kStages * SF_COLS <= kTmemCols, "TMEM budget");
 };
 
+// tmap_b: fp8 x fp4 only, the weight image as 4-bit codes {128 codes, 128
+// rows, N/128 * K/128 blocks}; unused otherwise.
 template <int MODE>
 __global__ void __launch_bounds__(kMxThreads, 1)
-    large_mx_kernel(const __grid_constant__ CUtensorMap tmap_a, const LargeParams p) {
+    large_mx_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_b,
+                    const LargeParams p) {
   using C = MxCfg<MODE>;
   extern __shared__ uint8_t dsmem[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(dsmem) + 1023) & ~uintptr_t(1023));
@@ -662,11 +669,17 @@ __global__ void __launch_bounds__(kMxThreads, 1)
     tmem_alloc(&tmem_base_sh, kTmemCols);
     tmem_relinquish();
   }
-  if (warp == 0 && lane == 0) prefetch_tmap(&tmap_a);
+  if (warp == 0 && lane == 0) {
+    prefetch_tmap(&tmap_a);
+    if (MODE == kMXFP4FP8A) prefetch_tmap(&tmap_b);
+  }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = tmem_base_sh;
+  // bytes one weight slab counts on the stage barrier: the packed fp4 block
+  // (8 KiB, written to 16 KiB of shared memory) or the 16 KiB slab
+  constexpr int kBSlabTx = MODE == kMXFP4FP8A ? 8192 : 16384;
 
   if (warp == 0) {
     if (lane == 0) {
@@ -684,7 +697,7 @@ __global__ void __launch_bounds__(kMxThreads, 1)
           uint8_t* st = smem + slot * C::STAGE_BYTES;
           const bool sf_here = !C::GROUP4 || (kb & 3) == 0;  // mxfp8: scales once per four slabs
           const int G = (KB + 3) / 4;
-          mbar_arrive_expect_tx(&full_bar[slot], kABytes + nslabs_n * 16384 +
+          mbar_arrive_expect_tx(&full_bar[slot], kABytes + nslabs_n * kBSlabTx +
                                                      (sf_here ? C::SFA_BYTES + nslabs_n * C::APS * 512 : 0));
           tma_load_2d(st, &tmap_a, kb * 128, tc.m * kBM, &full_bar[slot]);
           if (sf_here)
@@ -694,7 +707,10 @@ __global__ void __launch_bounds__(kMxThreads, 1)
                      C::SFA_BYTES, &full_bar[slot]);
           for (int h = 0; h < nslabs_n; ++h) {
             const size_t slab = static_cast<size_t>(2 * tc.n + h) * KB + kb;
-            bulk_g2s(st + kABytes + h * 16384, p.b_img + slab * 16384, 16384, &full_bar[slot]);
+            if (MODE == kMXFP4FP8A)
+              tma_load_3d(st + kABytes + h * 16384, &tmap_b, 0, 0, static_cast<int32_t>(slab), &full_bar[slot]);
+            else
+              bulk_g2s(st + kABytes + h * 16384, p.b_img + slab * 16384, 16384, &full_bar[slot]);
             if (sf_here) {
               const size_t atom = C::GROUP4 ? static_cast<size_t>(2 * tc.n + h) * G + kb / 4 : slab * C::APS;
               bulk_g2s(st + kABytes + kBBytes + C::SFA_BYTES + h * C::APS * 512, p.b_sf + atom * 512, C::APS * 512,
@@ -746,13 +762,17 @@ __global__ void __launch_bounds__(kMxThreads, 1)
             const uint64_t adesc = sdesc_sw128(smem_u32(st + j * 32));
             const uint64_t bdesc = sdesc_sw128(smem_u32(st + kABytes + j * 32));
             if (MODE == kMXFP8) {  // byte kb % 4 of the group's atoms
-              mma_mxf8f6f4(tmem, adesc, bdesc, idesc_mx(kBM, kBN, 0u, kb & 3, kb & 3), tmem + sfa, tmem + sfb,
+              mma_mxf8f6f4(tmem, adesc, bdesc, idesc_mx(kBM, kBN, kF8f6f4E4M3, kb & 3, kb & 3), tmem + sfa, tmem + sfb,
                            (kb | j) != 0);
             } else if (MODE == kMXFP8B32) {
-              mma_mxf8f6f4(tmem, adesc, bdesc, idesc_mx(kBM, kBN, 0u, j, j), tmem + sfa, tmem + sfb, (kb | j) != 0);
+              mma_mxf8f6f4(tmem, adesc, bdesc, idesc_mx(kBM, kBN, kF8f6f4E4M3, j, j), tmem + sfa, tmem + sfb,
+                           (kb | j) != 0);
+            } else if (MODE == kMXFP4FP8A) {
+              mma_mxf8f6f4(tmem, adesc, bdesc, idesc_mx_ab(kBM, kBN, kF8f6f4E4M3, kF8f6f4E2M1, j, j), tmem + sfa,
+                           tmem + sfb, (kb | j) != 0);
             } else {
               const int g = j >> 1, id = 2 * (j & 1);
-              mma_mxf4(tmem, adesc, bdesc, idesc_mx(kBM, kBN, 1u, id, id), tmem + sfa + 4 * g, tmem + sfb + 8 * g,
+              mma_mxf4(tmem, adesc, bdesc, idesc_mx(kBM, kBN, kMxf4E2M1, id, id), tmem + sfa + 4 * g, tmem + sfb + 8 * g,
                        (kb | j) != 0);
             }
           }
@@ -823,7 +843,8 @@ __global__ void __launch_bounds__(kMxThreads, 1)
 }
 
 template <int MODE>
-cudaError_t launch_mx(const CUtensorMap& tmap_a, const LargeParams& p, int ctas, cudaStream_t stream) {
+cudaError_t launch_mx(const CUtensorMap& tmap_a, const CUtensorMap& tmap_b, const LargeParams& p, int ctas,
+                      cudaStream_t stream) {
   static bool attr_set = false;
   if (!attr_set) {
     cudaError_t e = cudaFuncSetAttribute(large_mx_kernel<MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -831,7 +852,7 @@ cudaError_t launch_mx(const CUtensorMap& tmap_a, const LargeParams& p, int ctas,
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
-  large_mx_kernel<MODE><<<ctas, kMxThreads, MxCfg<MODE>::SMEM, stream>>>(tmap_a, p);
+  large_mx_kernel<MODE><<<ctas, kMxThreads, MxCfg<MODE>::SMEM, stream>>>(tmap_a, tmap_b, p);
   return cudaGetLastError();
 }
 
@@ -844,7 +865,8 @@ uint64_t large_streamk_bytes(int ctas, bool wide) {
 
 bool large_supported(int mode) { return mode == kBF16 || mode == kTensor || is_mx(mode); }
 
-cudaError_t launch_large(int mode, const CUtensorMap& tmap_a, const LargeParams& p, int ctas, cudaStream_t stream) {
+cudaError_t launch_large(int mode, const CUtensorMap& tmap_a, const CUtensorMap& tmap_b, const LargeParams& p,
+                         int ctas, cudaStream_t stream) {
   if (p.wide) {
     if (mode == kBF16) return launch_wide<kBF16>(tmap_a, p, ctas, stream);
     if (mode == kTensor) return launch_wide<kTensor>(tmap_a, p, ctas, stream);
@@ -852,9 +874,10 @@ cudaError_t launch_large(int mode, const CUtensorMap& tmap_a, const LargeParams&
   }
   if (mode == kBF16) return launch_mode<kBF16>(tmap_a, p, ctas, stream);
   if (mode == kTensor) return launch_mode<kTensor>(tmap_a, p, ctas, stream);
-  if (mode == kMXFP8) return launch_mx<kMXFP8>(tmap_a, p, ctas, stream);
-  if (mode == kMXFP8B32) return launch_mx<kMXFP8B32>(tmap_a, p, ctas, stream);
-  if (mode == kMXFP4) return launch_mx<kMXFP4>(tmap_a, p, ctas, stream);
+  if (mode == kMXFP8) return launch_mx<kMXFP8>(tmap_a, tmap_b, p, ctas, stream);
+  if (mode == kMXFP8B32) return launch_mx<kMXFP8B32>(tmap_a, tmap_b, p, ctas, stream);
+  if (mode == kMXFP4) return launch_mx<kMXFP4>(tmap_a, tmap_b, p, ctas, stream);
+  if (mode == kMXFP4FP8A) return launch_mx<kMXFP4FP8A>(tmap_a, tmap_b, p, ctas, stream);
   return cudaErrorNotSupported;
 }
 

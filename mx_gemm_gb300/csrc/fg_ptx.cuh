@@ -100,6 +100,16 @@ __device__ __forceinline__ void tma_load_2d(void* smem_dst, const CUtensorMap* m
       : "memory");
 }
 
+// 3-D tiled tensor copy (TMA) global -> shared (x as for tma_load_2d).
+__device__ __forceinline__ void tma_load_3d(void* smem_dst, const CUtensorMap* map, int32_t x, int32_t y, int32_t z,
+                                            uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4}], "
+      "[%5];" ::"r"(smem_u32(smem_dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(smem_u32(bar))
+      : "memory");
+}
+
 __device__ __forceinline__ void prefetch_tmap(const CUtensorMap* map) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }
@@ -332,33 +342,6 @@ __device__ __forceinline__ bool wait_flag_eq(const unsigned long long* flag, uns
   return true;
 }
 
-// ---------------------------------------------------- fp4 -> fp8 codes
-
-// The four e2m1 codes in the low 16 bits of w (code i in bits 4i..4i+3) as
-// four e4m3 codes (code i in byte i) of the same values: every e2m1 value is
-// an e4m3 value.  Magnitudes 0, 0.5, 1, 1.5, 2, 3, 4, 6 are e4m3 codes 0x00,
-// 0x30, 0x38, 0x3C, 0x40, 0x44, 0x48, 0x4C (selected by the 3 low bits of
-// each code); the sign moves from bit 3 of the code to bit 7 of the byte.
-__device__ __forceinline__ uint32_t e2m1x4_to_e4m3x4(uint32_t w) {
-  const uint32_t mag = __byte_perm(0x3C383000u, 0x4C484440u, w & 0x7777u);
-  uint32_t sg = w & 0x8888u;                 // sign of code i at bit 4i+3
-  sg = (sg | (sg << 8)) & 0x00880088u;       // codes 2, 3 to the upper half
-  sg = (sg | (sg << 4)) & 0x08080808u;       // code i's sign at bit 8i+3
-  return mag | (sg << 4);
-}
-
-// 16 bytes of packed e2m1 (32 codes, low nibble first) as 32 e4m3 bytes.
-__device__ __forceinline__ void e2m1x32_to_e4m3x32(uint4 q, uint4& lo, uint4& hi) {
-  lo.x = e2m1x4_to_e4m3x4(q.x);
-  lo.y = e2m1x4_to_e4m3x4(q.x >> 16);
-  lo.z = e2m1x4_to_e4m3x4(q.y);
-  lo.w = e2m1x4_to_e4m3x4(q.y >> 16);
-  hi.x = e2m1x4_to_e4m3x4(q.z);
-  hi.y = e2m1x4_to_e4m3x4(q.z >> 16);
-  hi.z = e2m1x4_to_e4m3x4(q.w);
-  hi.w = e2m1x4_to_e4m3x4(q.w >> 16);
-}
-
 // ------------------------------------------------------------- descriptors
 
 // Shared-memory matrix descriptor for a K-major operand stored in the
@@ -401,11 +384,18 @@ __host__ __device__ constexpr uint32_t idesc_e4m3(int M, int N) {
 }
 
 // Block-scaled kinds: B scale-factor byte id at bits 4-5, UE8M0 scale type
-// at bit 23, A scale-factor byte id at bits 29-30.  fmt is the element
-// format code of the kind (e4m3 = 0 for mxf8f6f4; e2m1 = 1 for mxf4).
-__host__ __device__ constexpr uint32_t idesc_mx(int M, int N, uint32_t fmt, uint32_t sfa_id, uint32_t sfb_id) {
-  return (sfb_id << 4) | (fmt << 7) | (fmt << 10) | (static_cast<uint32_t>(N >> 3) << 17) | (1u << 23) |
+// at bit 23, A scale-factor byte id at bits 29-30.  afmt / bfmt are the
+// element format codes of the kind: for mxf8f6f4 e4m3 = 0 and e2m1 = 5 (A
+// and B may differ; an e2m1 operand then sits in shared memory as 16 codes
+// in the low 8 bytes of each 16-byte chunk); for mxf4 e2m1 = 1 (packed).
+constexpr uint32_t kF8f6f4E4M3 = 0u, kF8f6f4E2M1 = 5u, kMxf4E2M1 = 1u;
+__host__ __device__ constexpr uint32_t idesc_mx_ab(int M, int N, uint32_t afmt, uint32_t bfmt, uint32_t sfa_id,
+                                                  uint32_t sfb_id) {
+  return (sfb_id << 4) | (afmt << 7) | (bfmt << 10) | (static_cast<uint32_t>(N >> 3) << 17) | (1u << 23) |
          (static_cast<uint32_t>(M >> 4) << 24) | (sfa_id << 29);
+}
+__host__ __device__ constexpr uint32_t idesc_mx(int M, int N, uint32_t fmt, uint32_t sfa_id, uint32_t sfb_id) {
+  return idesc_mx_ab(M, N, fmt, fmt, sfa_id, sfb_id);
 }
 
 }  // namespace fg

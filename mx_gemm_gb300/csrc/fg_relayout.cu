@@ -63,24 +63,6 @@ __global__ void block64_b_kernel(const uint4* __restrict__ src, uint4* __restric
   }
 }
 
-// Block64 fp4 image -> the 128-byte-swizzled e4m3 image of the same values
-// (slab (nb, kb) of 128 rows x 128 bytes at index nb*(K/128) + kb, chunk c
-// of row r at byte r*128 + ((c ^ (r%8))*16)).  One thread per packed chunk:
-// packed chunk c4 of row r (codes 32*c4 ..) becomes e4m3 chunks 2*c4, 2*c4+1.
-__global__ void expand_fp4_e4m3_kernel(const uint4* __restrict__ src, uint4* __restrict__ dst, int64_t chunks) {
-  for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < chunks;
-       i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
-    const int64_t blk = i >> 9;
-    const int c = static_cast<int>(i & 511);
-    const int r = c >> 2, c4 = c & 3;
-    uint4 lo, hi;
-    e2m1x32_to_e4m3x32(__ldg(src + i), lo, hi);
-    uint4* row = dst + blk * 1024 + r * 8;
-    row[(2 * c4) ^ (r & 7)] = lo;
-    row[(2 * c4 + 1) ^ (r & 7)] = hi;
-  }
-}
-
 // MX weight scales [N][K/blk] (E8M0 bytes) <-> atoms of 512 bytes whose byte
 // 16*(r%32) + 4*(r/32) + j belongs to row nb*128 + r.  mxfp4 and the 32-K
 // modes: for slab u and atom a of the slab, byte j is the scale of the 32-K
@@ -232,14 +214,6 @@ cudaError_t launch_block64_b(const uint8_t* src, uint8_t* dst, int64_t N, int64_
   if (work == 0) return cudaSuccess;
   block64_b_kernel<<<grid_for(work, 256), 256, 0, stream>>>(reinterpret_cast<const uint4*>(src),
                                                             reinterpret_cast<uint4*>(dst), N, Kb, inverse ? 1 : 0);
-  return cudaGetLastError();
-}
-
-cudaError_t launch_expand_fp4_e4m3(const uint8_t* src, uint8_t* dst, int64_t N, int64_t K, cudaStream_t stream) {
-  const int64_t chunks = N * (K / 2) / 16;
-  if (chunks == 0) return cudaSuccess;
-  expand_fp4_e4m3_kernel<<<grid_for(chunks, 256), 256, 0, stream>>>(reinterpret_cast<const uint4*>(src),
-                                                                    reinterpret_cast<uint4*>(dst), chunks);
   return cudaGetLastError();
 }
 

@@ -105,8 +105,10 @@ def test_plan_heuristic_and_table(fg):
     assert fg.gemm_workspace_size("fp8_tensor", 1, 2048, 7168, 4) == 0
     assert fg.gemm_workspace_size("fp8_tensor", 3, 2048, 7168, 16) == 16 * 3 * 2048 * 4
     assert fg.gemm_workspace_size("fp8_tensor", 1, 16384, 7168, 1) == 0
-    # large-M MX needs room for the per-call A scale image
+    # large-M MX needs room for the per-call A scale image (and nothing more:
+    # fp8 x fp4 reads its packed weights directly)
     assert fg.gemm_workspace_size("mxfp4", 4096, 16384, 7168) == 32 * 28 * 2 * 512
+    assert fg.gemm_workspace_size("mxfp4_fp8a", 4096, 16384, 7168) == 32 * 56 * 512
 
 
 def _fake_desc(fg, mode=1, N=128, K=128):
@@ -141,6 +143,11 @@ def test_preshuffle_argument_checks(fg):
     # misaligned B
     rc = L.fg_preshuffle_b(1, ctypes.c_void_p((1 << 20) + 8), ctypes.c_void_p(1 << 21), 128, 128,
                            ctypes.c_void_p(1 << 22), 128 * 128, ctypes.c_void_p(1 << 23), 16,
+                           ctypes.byref(out), None)
+    assert rc == fg.FG_ERR_ALIGN
+    # the fp4 image of fp8 x fp4 is read by a tensor copy that needs 32 bytes
+    rc = L.fg_preshuffle_b(fg.FG_MXFP4_FP8A, ctypes.c_void_p(1 << 20), ctypes.c_void_p(1 << 21), 128, 128,
+                           ctypes.c_void_p((1 << 22) + 16), 128 * 64, ctypes.c_void_p(1 << 23), 512,
                            ctypes.byref(out), None)
     assert rc == fg.FG_ERR_ALIGN
     # image too small
