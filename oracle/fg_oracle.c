@@ -345,7 +345,7 @@ int orc_unshuffle_b(const uint8_t *in, int64_t N, int64_t Kb, uint8_t *B)
  * The MXFP4_FP8A weight image: B as packed fp4 bytes, N rows of Kb = K/2
  * bytes, cut into blocks of 128 rows x 64 bytes (128 K of fp4), block
  * (nb, u) at index nb * (Kb/64) + u, row r of the block at byte r*64, no
- * swizzle.  (The kernel expands each block to e4m3 in shared memory itself.)
+ * swizzle.
  */
 int orc_block64_b(const uint8_t *B, int64_t N, int64_t Kb, uint8_t *out)
 {
