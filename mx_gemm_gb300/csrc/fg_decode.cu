@@ -101,6 +101,12 @@ struct DCfg {
   // bf16 and fp8-blockscale accumulate each K slab in its own TMEM partial
   // and fold the partials in registers (compensated), see the epilogue
   static constexpr bool PROMOTE = MODE == kBlock || MODE == kBF16;
+  // PROMOTE modes commit every slab's partial (pfull); when the partial
+  // buffers outnumber the slabs the MMA can run ahead of a waiting producer,
+  // ((STAGES - 1) * SPS + 1), that commit also tells the producer the stage
+  // is free, and the separate release commit (a few hundred cycles of the MMA
+  // pipe per stage) is left out
+  static constexpr bool PF_RELEASE = PROMOTE && NBUF >= (STAGES - 1) * SPS + 1;
   static constexpr int TMEM_NEED = PROMOTE ? NBUF * 16 : 32 + STAGES * 2 * SF_COLS;
   static constexpr int TMEM_COLS =
       TMEM_NEED <= 32 ? 32 : (TMEM_NEED <= 64 ? 64 : (TMEM_NEED <= 128 ? 128 : (TMEM_NEED <= 256 ? 256 : 512)));
@@ -195,7 +201,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (; it < niter; ++it) {
       const int slot = it % STAGES;
       const uint32_t ph = (it / STAGES) & 1;
-      const bool ok = mbar_wait(&empty_bar[slot], ph ^ 1u, T, p.err, 1);
+      bool ok = true;
+      if (!C::PF_RELEASE) {
+        ok = mbar_wait(&empty_bar[slot], ph ^ 1u, T, p.err, 1);
+      } else if (it >= STAGES) {
+        // the partial of the last slab of stage it - STAGES (slab commits
+        // arrive in order, so every earlier MMA of the stage is done too)
+        const int s_last = (it - STAGES + 1) * SPS - 1;
+        ok = mbar_wait(&pfull_bar[s_last % C::NBUF], (s_last / C::NBUF) & 1, T, p.err, 1);
+      }
       if (!__all_sync(0xffffffffu, ok)) {
         if (lane == 0) abort_sh = 1;
         break;
@@ -258,7 +272,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         // After an abort (it < niter) the signal goes out at once; the peers
         // then run out of time waiting for data that never comes.
         const int itf = niter - STAGES;
-        if (itf >= 0 && it == niter) mbar_wait(&empty_bar[niter % STAGES], (itf / STAGES) & 1, T, p.err, 9);
+        if (itf >= 0 && it == niter) {
+          if (C::PF_RELEASE) {
+            const int s_last = (itf + 1) * SPS - 1;
+            mbar_wait(&pfull_bar[s_last % C::NBUF], (s_last / C::NBUF) & 1, T, p.err, 9);
+          } else {
+            mbar_wait(&empty_bar[niter % STAGES], (itf / STAGES) & 1, T, p.err, 9);
+          }
+        }
         const int S = p.split;
         const int Mt = min(kTokRows, p.M - mt * kTokRows);
         const int myR = (128 * (split + 1) + S - 1) / S - (128 * split + S - 1) / S;
@@ -344,7 +365,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // (iteration it + STAGES) or, for the last such stage, the split-K
         // receive area.  A commit stalls the MMA pipe for about as long as
         // five of these MMAs, and the final commit covers the rest.
-        if (it + STAGES <= niter) tc_commit(&empty_bar[slot]);
+        if (!C::PF_RELEASE && it + STAGES <= niter) tc_commit(&empty_bar[slot]);
       }
       consumed_sh = it;
       if (ok && !C::PROMOTE) tc_commit(&acc_bar);
