@@ -226,16 +226,25 @@ def whole_job_value(steps, step_work, ms, world, unit_scale):
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "traffic.json")
 
 
+def _code_only(text):
+    """C/C++ source with its comments and all whitespace removed (string
+    literals kept), so that edits to comments leave the digest unchanged."""
+    import re
+    tok = re.compile(r'"(?:\\.|[^"\\])*"|//[^\n]*|/\*.*?\*/|\s+', re.S)
+    return tok.sub(lambda m: m.group(0) if m.group(0).startswith('"') else "", text)
+
+
 def kernel_sources_digest(fg):
-    """Digest of the library's kernel sources, to tell whether a stored ncu
-    traffic figure still describes the kernels being timed."""
+    """Digest of the library's kernel sources (code only, comments and
+    whitespace ignored), to tell whether a stored ncu traffic figure still
+    describes the kernels being timed."""
     import hashlib
     h = hashlib.sha256()
     csrc = os.path.join(os.path.dirname(fg.__file__), "csrc")
     for name in sorted(os.listdir(csrc)):
         if name.endswith((".cu", ".cuh")):
             h.update(name.encode())
-            h.update(open(os.path.join(csrc, name), "rb").read())
+            h.update(_code_only(open(os.path.join(csrc, name), encoding="utf-8").read()).encode())
     return h.hexdigest()[:16]
 
 

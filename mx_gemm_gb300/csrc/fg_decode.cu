@@ -61,9 +61,12 @@
 // (base + i/32).  tcgen05.cp.32x128b.warpx4 copies a 32-row x 16-byte
 // shared-memory atom into four TMEM columns of every 32-lane quarter, which
 // gives exactly that layout for atoms whose byte 16*(i%32) + 4*(i/32) + j
-// holds row i's scale for the j-th 32-K block.  For the 16 token rows only
-// lanes 0-15 of column 0 are read, so token atoms are laid out 256 bytes
-// apart and overlap (rows 16-31 of one atom are rows 0-15 of the next).
+// holds row i's scale for the j-th 32-K block.  For the 16 token rows the
+// MMA reads column 0 at lanes 32q + m (m < 16) of every quarter q -- which
+// the warpx4 copy fills from source rows 0-15 -- so token atoms are laid out
+// 256 bytes apart and overlap (rows 16-31 of one atom are rows 0-15 of the
+// next).  (A copy that filled the quarters from different rows gave wrong
+// token scales: quarters 1-3 are read too.)
 #include <cuda_bf16.h>
 
 #include <cstdio>
