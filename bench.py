@@ -33,34 +33,30 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 
 # ---------------------------------------------------------------- workloads
 
-def decode_cases(mode, K=7168):
-    return [dict(mode=mode, M=m, N=n, K=K) for m, n in inputs.DECODE_SHAPES]
+def _wl(src, first, n, kind):
+    """Cases first..first+n-1 of the seeded workload `src` of the inputs module
+    (its shapes, splits and seeds, shared with the parity tests)."""
+    cases = [dict(inputs.WORKLOADS[src]["cases"][first + i]) for i in range(n)]
+    return dict(cases=cases, kind=kind, src=src, first=first)
 
 
 WORKLOADS = {
-    "fp8_tensor_decode_sweep_k7168": dict(cases=decode_cases("fp8_tensor"), kind="decode", idx=1),
-    "large_bf16_54560x8192x8192": dict(cases=[dict(mode="bf16", M=54560, N=8192, K=8192)], kind="large", idx=3),
-    "large_fp8_4096x4096x8192": dict(cases=[dict(mode="fp8_tensor", M=4096, N=4096, K=8192)], kind="large",
-                                     idx=3, case_offset=1),
-    "fp8_block128_decode_sweep_k7168": dict(cases=decode_cases("fp8_block128"), kind="decode", idx=2),
-    "mxfp8_decode_n16384_k7168": dict(cases=[dict(mode="mxfp8", M=m, N=16384, K=7168) for m in (1, 16)],
-                                      kind="decode", idx=4),
-    "mxfp4_decode_n16384_k7168": dict(cases=[dict(mode="mxfp4", M=m, N=16384, K=7168) for m in (1, 16)],
-                                      kind="decode", idx=4, case_offset=3),
-    "mxfp8_b32_decode_n16384_k7168": dict(cases=[dict(mode="mxfp8_b32", M=m, N=16384, K=7168) for m in (1, 16)],
-                                          kind="decode", idx=5),
-    "bf16_decode_sweep_k7168": dict(cases=decode_cases("bf16"), kind="decode", idx=6),
-    "large_mxfp8_b32_4096x16384x7168": dict(cases=[dict(mode="mxfp8_b32", M=4096, N=16384, K=7168)], kind="large",
-                                            idx=5, case_offset=2),
-    "large_mxfp8_4096x16384x7168": dict(cases=[dict(mode="mxfp8", M=4096, N=16384, K=7168)], kind="large",
-                                        idx=4, case_offset=2),
-    "large_mxfp4_4096x16384x7168": dict(cases=[dict(mode="mxfp4", M=4096, N=16384, K=7168)], kind="large",
-                                        idx=4, case_offset=5),
+    # the pages' first decode configuration as stated: split_k fixed at 4
+    "fp8_tensor_decode_m1_n2048_k7168_split4": _wl("fp8_tensor_decode_m1_n2048_k7168_split4", 0, 1, "decode"),
+    "fp8_tensor_decode_sweep_k7168": _wl("fp8_tensor_decode_sweep_k7168", 0, 4, "decode"),
+    "large_bf16_54560x8192x8192": _wl("large_bf16_54560x8192x8192_fp8_4096x4096x8192", 0, 1, "large"),
+    "large_fp8_4096x4096x8192": _wl("large_bf16_54560x8192x8192_fp8_4096x4096x8192", 1, 1, "large"),
+    "fp8_block128_decode_sweep_k7168": _wl("fp8_block128_decode_sweep_k7168", 0, 4, "decode"),
+    "mxfp8_decode_n16384_k7168": _wl("mx_mxfp8_mxfp4_n16384_k7168", 0, 2, "decode"),
+    "mxfp4_decode_n16384_k7168": _wl("mx_mxfp8_mxfp4_n16384_k7168", 3, 2, "decode"),
+    "large_mxfp8_4096x16384x7168": _wl("mx_mxfp8_mxfp4_n16384_k7168", 2, 1, "large"),
+    "large_mxfp4_4096x16384x7168": _wl("mx_mxfp8_mxfp4_n16384_k7168", 5, 1, "large"),
+    "mxfp8_b32_decode_n16384_k7168": _wl("mx_mxfp8_b32_n16384_k7168", 0, 2, "decode"),
+    "large_mxfp8_b32_4096x16384x7168": _wl("mx_mxfp8_b32_n16384_k7168", 2, 1, "large"),
+    "bf16_decode_sweep_k7168": _wl("bf16_decode_sweep_k7168", 0, 4, "decode"),
     # fp8 activations against fp4 weights, on the MX shapes
-    "mxfp4_fp8a_decode_n16384_k7168": dict(cases=[dict(mode="mxfp4_fp8a", M=m, N=16384, K=7168) for m in (1, 16)],
-                                           kind="decode", idx=7),
-    "large_mxfp4_fp8a_4096x16384x7168": dict(cases=[dict(mode="mxfp4_fp8a", M=4096, N=16384, K=7168)],
-                                             kind="large", idx=7, case_offset=2),
+    "mxfp4_fp8a_decode_n16384_k7168": _wl("mx_fp8a_fp4w_n16384_k7168", 0, 2, "decode"),
+    "large_mxfp4_fp8a_4096x16384x7168": _wl("mx_fp8a_fp4w_n16384_k7168", 2, 1, "large"),
 }
 DEFAULT_WORKLOAD = "fp8_tensor_decode_sweep_k7168"
 MX_MODES = ("mxfp8", "mxfp4", "mxfp8_b32", "mxfp4_fp8a")
@@ -103,10 +99,9 @@ def work(kind, c, n=None):
 METRIC = {"decode": ("decode GEMM GB/s", "GB/s", 1e9), "large": ("large GEMM TFLOP/s", "TFLOP/s", 1e12)}
 
 
-def case_operands(wl_idx, i, c):
-    off = 10 * i
-    return inputs.operands(c["mode"], c["M"], c["N"], c["K"], 1000 + wl_idx + off, 2000 + wl_idx + off,
-                           3000 + wl_idx + off)
+def case_operands(wl, i):
+    """Host operands of case i of a bench workload (seeded as in the inputs module)."""
+    return inputs.workload_operands(wl["src"], wl["first"] + i)
 
 
 # ------------------------------------------------------------------ clocks
@@ -165,24 +160,33 @@ class ClockSampler:
 # ------------------------------------------------------------- oracle arm
 
 class OracleSample:
-    """The oracle on a sample of each case: the first n weight rows (all M rows,
-    full K), n the same fraction of N for every case, calibrated once so that
-    one pass costs about target_s seconds."""
+    """The oracle on a bounded sample of each case, calibrated once so that one
+    pass costs about target_s seconds on `threads` host threads.
 
-    def __init__(self, wl, host_ops, target_s):
+    Decode cases (M <= 32): all M rows against the first n weight rows (full
+    K).  Large cases: the 256 seeded sample rows of A (rows 0 and M-1
+    included, as in the parity tests) against the first n weight rows.  n is
+    the same fraction of N for every case.  The rate (work / time) is what is
+    reported; full-step times are extrapolated from it and labelled so."""
+
+    def __init__(self, wl, host_ops, target_s, threads=None):
         import oracle
         self.oracle = oracle
         self.orc = {"bf16": oracle.BF16, "fp8_tensor": oracle.FP8_TENSOR, "fp8_block128": oracle.FP8_BLOCK128,
                     "mxfp8": oracle.MXFP8, "mxfp4": oracle.MXFP4, "mxfp8_b32": oracle.MXFP8_B32,
                     "mxfp4_fp8a": oracle.MXFP4_FP8A}
         self.wl, self.host_ops = wl, host_ops
-        self.threads = os.cpu_count() or 1
-        self.frac = 1.0 / 1024
+        self.threads = threads or os.cpu_count() or 1
+        self.large = wl["kind"] == "large"
+        self.frac = 1.0 / 4096
         t, _ = self.run()
-        self.frac = min(1.0, max(1.0 / 1024, self.frac * target_s / max(t, 1e-6)))
+        self.frac = min(1.0, max(1.0 / 4096, self.frac * target_s / max(t, 1e-6)))
 
     def rows(self, c):
         return max(8, int(c["N"] * self.frac) // 8 * 8)
+
+    def a_rows(self, c):
+        return inputs.sample_rows(c["M"]) if self.large else None
 
     def run(self):
         t0 = time.perf_counter()
@@ -194,14 +198,40 @@ class OracleSample:
                 bs = b_s[: (n + 127) // 128]
             elif c["mode"] in MX_MODES:
                 bs = b_s[:n]
-            self.oracle.gemm(self.orc[c["mode"]], A, B[:n], a_s, bs, M=c["M"], N=n, K=c["K"],
+            rows = self.a_rows(c)
+            self.oracle.gemm(self.orc[c["mode"]], A, B[:n], a_s, bs, M=c["M"], N=n, K=c["K"], rows=rows,
                              threads=self.threads)
-            nbytes += work(self.wl["kind"], c, n)
+            m = c["M"] if rows is None else len(rows)
+            nbytes += work(self.wl["kind"], dict(c, M=m), n)
         return time.perf_counter() - t0, nbytes
 
     def describe(self):
-        return "first %s weight rows of the %s cases (all M rows, full K) per pass" % (
-            "/".join(str(self.rows(c)) for c in self.wl["cases"]), len(self.wl["cases"]))
+        what = "the 256 seeded sample rows of A" if self.large else "all M rows"
+        return "first %s weight rows of the %s cases (%s, full K) per pass, %d host thread%s" % (
+            "/".join(str(self.rows(c)) for c in self.wl["cases"]), len(self.wl["cases"]), what,
+            self.threads, "" if self.threads == 1 else "s")
+
+
+def cpu_baseline(wl, host_ops, kind, unit, scale_u, step_work):
+    """The oracle timed on the host cores twice -- single-threaded and on every
+    core -- each on its own calibrated sample; value = the all-core rate."""
+    out = {}
+    for label, threads, target in (("all_cores", os.cpu_count() or 1, 10.0), ("single_thread", 1, 6.0)):
+        ref = OracleSample(wl, host_ops, target, threads)
+        t, nw = ref.run()
+        rate = nw / t
+        out[label] = {"value": rate / scale_u, "unit": unit, "cores": threads,
+                      "sample": ref.describe() + ", one pass of %.1f s" % t,
+                      "full_step_s_extrapolated": step_work / rate}
+    allc = out["all_cores"]
+    return {"value": allc["value"], "unit": unit, "cores": allc["cores"], "kind": "oracle",
+            "sample": allc["sample"], "single_thread": out["single_thread"],
+            "full_step_s_extrapolated": {
+                "all_cores": allc["full_step_s_extrapolated"],
+                "single_thread": out["single_thread"]["full_step_s_extrapolated"],
+                "how": "EXTRAPOLATED, not measured: sample time x (work of one full step / work of the "
+                       "sample)%s" % (" (x M/256 for the rows of A)" if kind == "large" else "")},
+            "host_cores": os.cpu_count()}
 
 
 # ---------------------------------------------------------- multi-rank
@@ -294,8 +324,7 @@ def main():
             peaks_src = "measured"
         except ValueError:
             pass
-    off = wl.get("case_offset", 0)
-    host_ops_fn = lambda: [case_operands(wl["idx"], i + off, c) for i, c in enumerate(wl["cases"])]  # noqa: E731
+    host_ops_fn = lambda: [case_operands(wl, i) for i in range(len(wl["cases"]))]  # noqa: E731
     dtype = {"bf16": "bf16", "fp8_tensor": "e4m3", "fp8_block128": "e4m3", "mxfp8": "e4m3",
              "mxfp4": "e2m1", "mxfp8_b32": "e4m3", "mxfp4_fp8a": "e4m3xe2m1"}[wl["cases"][0]["mode"]]
 
@@ -354,9 +383,9 @@ def main():
         del dB
         dA0 = to_dev(A)
         dAs = [dA0] + [dA0.clone() for _ in range(R - 1 if kind == "large" else 0)]
-        plan = fg.gemm_plan(c["mode"], c["M"], c["N"], c["K"])
+        plan = fg.gemm_plan(c["mode"], c["M"], c["N"], c["K"], c.get("split_k", 0))
         S = plan["split_k"]
-        ws_bytes = fg.gemm_workspace_size(c["mode"], c["M"], c["N"], c["K"])
+        ws_bytes = fg.gemm_workspace_size(c["mode"], c["M"], c["N"], c["K"], S)
         ws = torch.empty(max(4, ws_bytes) // 4, dtype=torch.float32, device=dev)
         Y = torch.empty((c["M"], c["N"]), dtype=torch.bfloat16, device=dev)
         hA = torch.from_numpy(np.ascontiguousarray(A).view(np.int16) if A.dtype == np.uint16 else
@@ -447,6 +476,25 @@ def main():
                          "split_k": x["S"], "kernel": x["plan"]["name"], "us": round(avg * 1e3, 3),
                          unit.replace("/", "p"): round(x["work"] / (avg / 1e3) / scale_u, 1)})
     achieved = step_work / (sum(main_ms) / 1e3) / scale_u
+    if kind == "decode":
+        # The shape's own bandwidth wall: a device-to-device copy whose read +
+        # write bytes equal the GEMM's algorithmic bytes, timed the same way
+        # (back to back in a graph, cycling through buffers larger than twice
+        # the L2), so each shape's GB/s sits beside what a plain stream of the
+        # same size reaches.
+        for x, pc in zip(cases, per_case):
+            nb = max(16, x["work"] // 2 // 16 * 16)
+            R = max(2, -(-2 * l2_bytes // nb) + 1)
+            src = [torch.empty(nb, dtype=torch.uint8, device=dev) for _ in range(R)]
+            dst = [torch.empty(nb, dtype=torch.uint8, device=dev) for _ in range(R)]
+            n = max(20, min(K, 400))
+            g = graph_of(lambda r: dst[r % R].copy_(src[(r + 1) % R]), n)
+            cms = time_graph(g) / n
+            del g, src, dst
+            copy_gbs = 2 * nb / (cms / 1e3) / 1e9
+            pc["copy_us"] = round(cms * 1e3, 3)
+            pc["copy_GBps"] = round(copy_gbs, 1)
+            pc["frac_of_copy"] = round(pc["GBps"] / copy_gbs, 4)
     if kind == "decode":
         bound, peak, psrc = "hbm", float(peaks["hbm_gbs"]), peaks_src + " hbm_gbs (burst copy)"
     else:
@@ -583,10 +631,7 @@ def main():
 
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
-        ref = OracleSample(wl, host_ops, 15.0)
-        t, nw = ref.run()
-        cpu = {"value": nw / t / scale_u, "unit": unit, "cores": ref.threads, "kind": "oracle",
-               "sample": ref.describe() + ", one pass of %.1f s" % t}
+        cpu = cpu_baseline(wl, host_ops, kind, unit, scale_u, step_work)
 
     if rank == 0:
         wbytes = sum(x["c"]["N"] * x["c"]["K"] * elem_bytes(x["c"]["mode"]) for x in cases)

@@ -113,12 +113,13 @@ typedef enum fg_mode {
  * only the packed bytes.
  *
  * Scale image (sf): FP8_TENSOR: the fp32 b_s (16 bytes reserved);
- * FP8_BLOCK128: b_s fp32 [N/128][K/128] unchanged; MXFP8 / MXFP8_B32 /
- * MXFP4_FP8A (one atom per 128 K) / MXFP4: for each 128-row tile and slab,
- * 1 (8-bit) or 2 (MXFP4) atoms of 512
- * bytes, atom byte 16*(r%32) + 4*(r/32) + j = the E8M0 of row r for the j-th
- * 32-K block the atom covers (an MXFP8 128-K scale repeated for its four
- * 32-K blocks); BF16: none.
+ * FP8_BLOCK128: b_s fp32 [N/128][K/128] unchanged; MXFP8_B32 / MXFP4_FP8A
+ * (one atom per 128 K) / MXFP4 (two atoms per 256 K): for each 128-row tile
+ * and slab, atoms of 512 bytes, atom byte 16*(r%32) + 4*(r/32) + j = the
+ * E8M0 of row r for the j-th 32-K block the atom covers; MXFP8 (one scale
+ * per 128 K): one atom per four consecutive 128-K slabs of a 128-row tile,
+ * byte j of row r = the E8M0 of slab 4g + j (zero past the last slab);
+ * BF16: none.
  */
 typedef struct fg_bshuf {
   uint32_t magic;
@@ -247,22 +248,34 @@ FG_API fg_status fg_gemm_splitk_reduce(const float* ws, int split_k, int64_t M, 
  * callers that cannot allocate device memory while they run -- a serving
  * loop whose buffers are all sized at start-up (cudaMalloc can synchronise
  * the device and stall every stream), or a plug-in whose host framework owns
- * all device memory and offers no allocator.  The fp32 split-K partials go
- * to an 8 MiB array that the library keeps in every device's memory until
- * the process exits (used by calls whose split needs a workspace, i.e.
- * splits above 8); this call allocates nothing.
+ * all device memory and offers no allocator.  Whatever fg_gemm would keep in
+ * a caller workspace goes to one 8 MiB array that the library keeps in every
+ * device's memory until the process exits; this call allocates nothing.
+ * The array holds, depending on the call:
+ *  - the fp32 split-K partials of a split above 8 (splits 9..16):
+ *    split_k * M * N * 4 bytes, refused with FG_ERR_WORKSPACE (before
+ *    anything is launched) when above 8 MiB;
+ *  - the A scale image of a large-M MX call (M > 32, MX modes):
+ *    M/128 rounded up * K/128 * 512 bytes (twice that for MXFP4; a quarter,
+ *    rounded up, for MXFP8), refused with FG_ERR_WORKSPACE when above 8 MiB;
+ *  - the optional stream-K partials and flags of a large-M bf16 / fp8 call,
+ *    when they fit (about 128 KiB per CTA for 128 x 256 tiles, 256 KiB for
+ *    256 x 256 tiles; more than 8 MiB once the grid has more than 63 / 31
+ *    CTAs).  When they do not fit the call is not refused: every tile then
+ *    runs whole, as fg_gemm does with a smaller workspace.
+ * Splits of 2..8 and split 1 need no scratch.
  *  - Arguments as fg_gemm, minus the workspace.  FG_FLAG_DEFER_REDUCE is
  *    refused (FG_ERR_INVALID_ARG): the partials would stay in the private
  *    scratch.
- *  - A call whose split needs more than 8 MiB (split_k * M * N * 4 bytes) is
- *    refused with FG_ERR_WORKSPACE before anything is launched.
  *  - The first call on a device looks up the scratch's device address (once
  *    per device, with that device current); make that first call before any
  *    stream capture.
- *  - All calls share the one array and it keeps the last call's partials.
+ *  - All calls share the one array and it keeps the last call's contents.
  *    Nothing in it has to start at zero (every split writes its whole
- *    partial before the reduce reads it), but two calls that overlap on the
- *    GPU (e.g. on two streams) race on it: serialise them.
+ *    partial before the reduce reads it, every large-M MX call rewrites its
+ *    whole A scale image, a stream-K flag matches only the launch that wrote
+ *    it), but two calls that overlap on the GPU (e.g. on two streams) race on
+ *    it: serialise them.
  * Errors: as fg_gemm.
  */
 FG_API fg_status fg_gemm_noalloc(const void* A, const void* a_scales, int64_t M, const fg_bshuf* b, int mode,

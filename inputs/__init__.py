@@ -193,9 +193,14 @@ WORKLOADS = {
     "mx_mxfp8_mxfp4_n16384_k7168": dict(
         idx=4, cases=[dict(mode=f, M=m, N=16384, K=7168, split_k=0)
                       for f in ("mxfp8", "mxfp4") for m in (1, 16, 4096)]),
-    # next: fp8 activations against fp4 weights (the MX shapes above)
+    # next rows: the OCP 32-element mxfp8 block, the bf16 decode sweep, and
+    # fp8 activations against fp4 weights (on the MX shapes above)
+    "mx_mxfp8_b32_n16384_k7168": dict(
+        idx=5, cases=[dict(mode="mxfp8_b32", M=m, N=16384, K=7168, split_k=0) for m in (1, 16, 4096)]),
+    "bf16_decode_sweep_k7168": dict(
+        idx=6, cases=[dict(mode="bf16", M=m, N=n, K=7168, split_k=0) for m, n in DECODE_SHAPES]),
     "mx_fp8a_fp4w_n16384_k7168": dict(
-        idx=5, cases=[dict(mode="mxfp4_fp8a", M=m, N=16384, K=7168, split_k=0) for m in (1, 16, 4096)]),
+        idx=7, cases=[dict(mode="mxfp4_fp8a", M=m, N=16384, K=7168, split_k=0) for m in (1, 16, 4096)]),
 }
 
 

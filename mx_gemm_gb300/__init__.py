@@ -104,6 +104,93 @@ def _ptr(t):
     return None if t is None else ctypes.c_void_p(t.data_ptr())
 
 
+# ----------------------------------------------------------- argument checks
+# The C ABI sees raw bytes: a transposed or sliced view, a tensor on another
+# device or of another element type would be read as if it were the row-major
+# operand.  These checks (no arithmetic) refuse such tensors with ValueError.
+
+def _dtypes(*names):
+    return tuple(getattr(torch, n) for n in names if hasattr(torch, n))
+
+
+_BYTES = _dtypes("uint8", "int8")
+_BF16 = _dtypes("bfloat16", "int16", "uint16")
+_FP8 = _BYTES + _dtypes("float8_e4m3fn")
+_FP4 = _BYTES + _dtypes("float4_e2m1fn_x2")
+_E8M0 = _BYTES + _dtypes("float8_e8m0fnu")
+_F32 = (torch.float32,)
+
+
+def _a_dtypes(mode):
+    return {FG_BF16: _BF16, FG_MXFP4: _FP4}.get(mode, _FP8)
+
+
+def _b_dtypes(mode):
+    return {FG_BF16: _BF16, FG_MXFP4: _FP4, FG_MXFP4_FP8A: _FP4}.get(mode, _FP8)
+
+
+def _a_row_bytes(mode, K):
+    return {FG_BF16: 2 * K, FG_MXFP4: K // 2}.get(mode, K)
+
+
+def _b_row_bytes(mode, K):
+    return K // 2 if mode == FG_MXFP4_FP8A else _a_row_bytes(mode, K)
+
+
+def _scale_spec(mode, rows, K, is_b):
+    """(dtypes, element count) of the scales of an operand with `rows` rows."""
+    if mode == FG_FP8_TENSOR:
+        return _F32, 1
+    if mode == FG_FP8_BLOCK128:
+        return _F32, ((rows // 128) if is_b else rows) * (K // 128)
+    if mode == FG_MXFP8:
+        return _E8M0, rows * (K // 128)
+    if mode in (FG_MXFP4, FG_MXFP8_B32, FG_MXFP4_FP8A):
+        return _E8M0, rows * (K // 32)
+    return None, 0
+
+
+def _require(t, name, dtypes=None, device=None, shape=None, numel=None, min_numel=None):
+    if not isinstance(t, torch.Tensor):
+        raise ValueError("%s must be a torch.Tensor, got %s" % (name, type(t).__name__))
+    if not t.is_contiguous():
+        raise ValueError("%s must be contiguous row-major memory (shape %s, strides %s): a transposed or "
+                         "column-sliced view would be read as raw bytes" % (name, tuple(t.shape), t.stride()))
+    if not t.is_cuda:
+        raise ValueError("%s must be a CUDA tensor (it is on %s)" % (name, t.device))
+    if device is not None and t.device != device:
+        raise ValueError("%s is on %s, the other operands on %s" % (name, t.device, device))
+    if dtypes is not None and t.dtype not in dtypes:
+        raise ValueError("%s has dtype %s; expected one of %s" % (name, t.dtype, ", ".join(str(d) for d in dtypes)))
+    if shape is not None and tuple(t.shape) != tuple(shape):
+        raise ValueError("%s has shape %s, expected %s" % (name, tuple(t.shape), tuple(shape)))
+    if numel is not None and t.numel() != numel:
+        raise ValueError("%s has %d elements, expected %d" % (name, t.numel(), numel))
+    if min_numel is not None and t.numel() < min_numel:
+        raise ValueError("%s has %d elements, needs at least %d" % (name, t.numel(), min_numel))
+
+
+def _row_bytes_of(t):
+    return t.shape[1] * t.element_size() if t.dim() == 2 else -1
+
+
+def _check_gemm_args(mode, A, pb, a_scales, Y):
+    dev = pb.data.device
+    _require(A, "A", _a_dtypes(mode), dev)
+    M = A.shape[0] if A.dim() == 2 else -1
+    if A.dim() != 2 or _row_bytes_of(A) != _a_row_bytes(mode, pb.K):
+        raise ValueError("A must be [M][K] codes of the mode (%d bytes per row for K=%d), got shape %s dtype %s"
+                         % (_a_row_bytes(mode, pb.K), pb.K, tuple(A.shape), A.dtype))
+    # a missing scale tensor or a mode that differs from the weight's is the
+    # library's to report (FG_ERR_INVALID_ARG / FG_ERR_LAYOUT)
+    if a_scales is not None and mode == pb.mode and mode != FG_BF16:
+        dts, n = _scale_spec(mode, M, pb.K, False)
+        _require(a_scales, "a_scales", dts, dev, numel=n)
+    if Y is not None:
+        _require(Y, "Y", _dtypes("bfloat16", "int16"), dev, shape=(M, pb.N))
+    return M
+
+
 def _stream(stream):
     if stream is None:
         return ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
@@ -154,9 +241,18 @@ def preshuffle_b(mode, B, b_scales=None, K=None, stream=None):
     """One-time relayout of weight B (device tensor [N][K] bf16 / uint8 codes /
     packed fp4 [N][K/2]) and its scales; returns a PreshuffledB."""
     mode = _mode(mode)
+    _require(B, "B", _b_dtypes(mode))
+    if B.dim() != 2:
+        raise ValueError("B must be 2-D [N][K] codes, got shape %s" % (tuple(B.shape),))
     N = B.shape[0]
+    rb = _row_bytes_of(B)
     if K is None:
-        K = B.shape[1] * (2 if mode in (FG_MXFP4, FG_MXFP4_FP8A) else 1)
+        K = {FG_BF16: rb // 2, FG_MXFP4: 2 * rb, FG_MXFP4_FP8A: 2 * rb}.get(mode, rb)
+    if rb != _b_row_bytes(mode, K):
+        raise ValueError("B has %d bytes per row; K=%d needs %d" % (rb, K, _b_row_bytes(mode, K)))
+    if b_scales is not None and mode != FG_BF16:
+        dts, n = _scale_spec(mode, N, K, True)
+        _require(b_scales, "b_scales", dts, B.device, numel=n)
     nb, ns = preshuffle_b_size(mode, N, K)
     data = torch.empty(nb, dtype=torch.uint8, device=B.device)
     sf = torch.empty(max(ns, 16), dtype=torch.uint8, device=B.device) if ns else None
@@ -206,9 +302,11 @@ def gemm(A, pb, a_scales=None, mode=None, split_k=0, Y=None, workspace=None, fla
     one and none is given.  Returns Y.
     """
     mode = pb.mode if mode is None else _mode(mode)
-    M = A.shape[0]
+    M = _check_gemm_args(mode, A, pb, a_scales, Y)
     if Y is None:
         Y = torch.empty((M, pb.N), dtype=torch.bfloat16, device=A.device)
+    if workspace is not None:
+        _require(workspace, "workspace", device=A.device)
     ws_bytes = 0
     if workspace is None:
         need = gemm_workspace_size(mode, M, pb.N, pb.K, split_k) if M > 0 else 0
@@ -221,19 +319,27 @@ def gemm(A, pb, a_scales=None, mode=None, split_k=0, Y=None, workspace=None, fla
     return Y
 
 
-def gemm_noalloc(A, pb, a_scales=None, mode=None, split_k=0, Y=None, flags=0, stream=None):
-    """gemm() for callers that cannot allocate device memory: the split-K
-    partials go to the library's built-in 8 MiB scratch (see fg_gemm_noalloc
-    in include/fg.h).  Y must be given by such a caller; returns Y."""
+def gemm_noalloc(A, pb, Y, a_scales=None, mode=None, split_k=0, flags=0, stream=None):
+    """gemm() for callers that cannot allocate device memory: whatever would
+    need a workspace goes to the library's built-in 8 MiB scratch (see
+    fg_gemm_noalloc in include/fg.h).  The caller passes Y (this wrapper
+    allocates nothing either); returns Y."""
     mode = pb.mode if mode is None else _mode(mode)
     if Y is None:
-        Y = torch.empty((A.shape[0], pb.N), dtype=torch.bfloat16, device=A.device)
+        raise ValueError("gemm_noalloc needs the caller's output Y (it allocates nothing)")
+    _check_gemm_args(mode, A, pb, a_scales, Y)
     _check(lib().fg_gemm_noalloc(_ptr(A), _ptr(a_scales), A.shape[0], ctypes.byref(pb.desc), mode, split_k,
                                  _ptr(Y), flags, _stream(stream)))
     return Y
 
 
 def gemm_splitk_reduce(ws, split_k, M, N, a_s=None, b_s=None, Y=None, stream=None):
+    _require(ws, "ws", _F32, min_numel=split_k * M * N)
+    for name, t in (("a_s", a_s), ("b_s", b_s)):
+        if t is not None:
+            _require(t, name, _F32, ws.device, numel=1)
+    if Y is not None:
+        _require(Y, "Y", _dtypes("bfloat16", "int16"), ws.device, shape=(M, N))
     if Y is None:
         Y = torch.empty((M, N), dtype=torch.bfloat16, device=ws.device)
     _check(lib().fg_gemm_splitk_reduce(_ptr(ws), split_k, M, N, _ptr(a_s), _ptr(b_s), _ptr(Y),

@@ -19,6 +19,8 @@
 #include <cstring>
 #include <ctime>
 #include <mutex>
+#include <utility>
+#include <vector>
 
 #include "../../include/fg.h"
 #include "fg_internal.cuh"
@@ -347,6 +349,20 @@ void set_error_message(const char* fmt, ...) {
   va_start(ap, fmt);
   vsnprintf(g_msg, sizeof g_msg, fmt, ap);
   va_end(ap);
+}
+
+cudaError_t ensure_smem_attr(const void* kernel, int bytes) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  static std::mutex mu;
+  static std::vector<std::pair<const void*, int>> done;  // (kernel, device) pairs already set
+  std::lock_guard<std::mutex> lock(mu);
+  for (const auto& d : done)
+    if (d.first == kernel && d.second == dev) return cudaSuccess;
+  e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e == cudaSuccess) done.emplace_back(kernel, dev);
+  return e;
 }
 
 int sm_count() {

@@ -595,13 +595,8 @@ template <int MODE, int SPS, int STAGES>
 cudaError_t launch_one(const CUtensorMap& tmap_a, const CUtensorMap& tmap_b, const DecodeParams& p, dim3 grid,
                        cudaStream_t stream) {
   using C = DCfg<MODE, SPS, STAGES>;
-  static bool attr_set = false;  // per process; the attribute applies to every device
-  if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(decode_kernel<MODE, SPS, STAGES>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
-    if (e != cudaSuccess) return e;
-    attr_set = true;
-  }
+  cudaError_t e = ensure_smem_attr(reinterpret_cast<const void*>(&decode_kernel<MODE, SPS, STAGES>), C::SMEM);
+  if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = grid;
   cfg.blockDim = dim3(kThreads);

@@ -108,6 +108,10 @@ cudaError_t launch_reduce(const float* ws, int split, int64_t M, int64_t N, cons
 
 int sm_count();
 
+// Raise a kernel's dynamic shared-memory limit to `bytes` on the current
+// device, once per (kernel, device) pair; thread-safe.
+cudaError_t ensure_smem_attr(const void* kernel, int bytes);
+
 // Programmatic dependent launch is on unless FG_NO_PDL is set (a sweep hook
 // for measuring what the overlap is worth).
 bool pdl_enabled();

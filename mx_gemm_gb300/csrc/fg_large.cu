@@ -310,12 +310,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 template <int MODE>
 cudaError_t launch_mode(const CUtensorMap& tmap_a, const LargeParams& p, int ctas, cudaStream_t stream) {
-  static bool attr_set = false;
-  if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(large_kernel<MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
-    if (e != cudaSuccess) return e;
-    attr_set = true;
-  }
+  cudaError_t e = ensure_smem_attr(reinterpret_cast<const void*>(&large_kernel<MODE>), kSmem);
+  if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(ctas);
   cfg.blockDim = dim3(kThreads);
@@ -574,13 +570,8 @@ __global__ void __launch_bounds__(kWideThreads, 1)
 
 template <int MODE>
 cudaError_t launch_wide(const CUtensorMap& tmap_a, const LargeParams& p, int ctas, cudaStream_t stream) {
-  static bool attr_set = false;
-  if (!attr_set) {
-    cudaError_t e =
-        cudaFuncSetAttribute(large_wide_kernel<MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize, kWideSmem);
-    if (e != cudaSuccess) return e;
-    attr_set = true;
-  }
+  cudaError_t e = ensure_smem_attr(reinterpret_cast<const void*>(&large_wide_kernel<MODE>), kWideSmem);
+  if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(ctas);
   cfg.blockDim = dim3(kWideThreads);
@@ -845,13 +836,8 @@ __global__ void __launch_bounds__(kMxThreads, 1)
 template <int MODE>
 cudaError_t launch_mx(const CUtensorMap& tmap_a, const CUtensorMap& tmap_b, const LargeParams& p, int ctas,
                       cudaStream_t stream) {
-  static bool attr_set = false;
-  if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(large_mx_kernel<MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         MxCfg<MODE>::SMEM);
-    if (e != cudaSuccess) return e;
-    attr_set = true;
-  }
+  cudaError_t e = ensure_smem_attr(reinterpret_cast<const void*>(&large_mx_kernel<MODE>), MxCfg<MODE>::SMEM);
+  if (e != cudaSuccess) return e;
   large_mx_kernel<MODE><<<ctas, kMxThreads, MxCfg<MODE>::SMEM, stream>>>(tmap_a, tmap_b, p);
   return cudaGetLastError();
 }

@@ -67,13 +67,30 @@ extern "C" FG_API fg_status fg_gemm_noalloc(const void* A, const void* a_scales,
                           "private scratch; use fg_gemm with a workspace");
     return FG_ERR_INVALID_ARG;
   }
-  if (b && b->magic == FG_BSHUF_MAGIC && b->version == FG_BSHUF_VERSION) {
+  if (b && b->magic == FG_BSHUF_MAGIC && b->version == FG_BSHUF_VERSION && M > 0) {
+    // Only what fg_gemm cannot do without is checked against the scratch:
+    // the fp32 partials of a split above the cluster limit, and the A scale
+    // image of the large-M MX kernel.  The large-M bf16 / fp8 kernel's
+    // stream-K buffer is optional: when it does not fit, fg_gemm runs every
+    // tile whole.
+    fg_plan plan;
     uint64_t need = 0;
-    if (fg_gemm_workspace_size(mode, M, b->N, b->K, split_k, &need) == FG_OK && need > kScratchBytes) {
-      fg::set_error_message("fg_gemm_noalloc: split_k*M*N*4 = %llu bytes of split-K partials exceed the %llu-byte "
-                            "built-in scratch; use a smaller split_k or fg_gemm with a caller workspace",
-                            (unsigned long long)need, kScratchBytes);
-      return FG_ERR_WORKSPACE;
+    if (fg_gemm_plan(mode, M, b->N, b->K, split_k, &plan) == FG_OK &&
+        fg_gemm_workspace_size(mode, M, b->N, b->K, split_k, &need) == FG_OK) {
+      const bool large_mx = plan.path == 1 && mode != FG_BF16 && mode != FG_FP8_TENSOR;
+      if (plan.path == 0 && need > kScratchBytes) {
+        fg::set_error_message("fg_gemm_noalloc: split_k=%d needs split_k*M*N*4 = %llu bytes of fp32 partials, more "
+                              "than the %llu-byte built-in scratch; use a split of at most 8 (no partials in "
+                              "memory), a smaller split, or fg_gemm with a caller workspace",
+                              plan.split_k, (unsigned long long)need, kScratchBytes);
+        return FG_ERR_WORKSPACE;
+      }
+      if (large_mx && need > kScratchBytes) {
+        fg::set_error_message("fg_gemm_noalloc: the large-M MX kernel's A scale image takes %llu bytes for M=%lld, "
+                              "more than the %llu-byte built-in scratch; use fg_gemm with a caller workspace",
+                              (unsigned long long)need, (long long)M, kScratchBytes);
+        return FG_ERR_WORKSPACE;
+      }
     }
   }
   cudaError_t e = cudaSuccess;
@@ -84,6 +101,7 @@ extern "C" FG_API fg_status fg_gemm_noalloc(const void* A, const void* a_scales,
   }
   // fg_gemm does every other check.  No part of the scratch has to start at
   // zero: each split writes all of its [M][N] partial before the reduce
-  // reads it.
+  // reads it, the A scale image is rewritten whole by every large-M MX call,
+  // and a stream-K flag only matches the launch that wrote it.
   return fg_gemm(A, a_scales, M, b, mode, split_k, Y, scratch, kScratchBytes, flags, stream);
 }

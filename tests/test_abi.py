@@ -195,3 +195,28 @@ def test_decode_config_override_is_validated(fg, monkeypatch):
         with pytest.raises(fg.FgError) as e:
             fg.gemm_plan("fp8_tensor", 1, 2048, 7168)
         assert e.value.status == fg.FG_ERR_INVALID_ARG
+
+
+def test_binding_refuses_views_and_host_tensors(fg):
+    """The binding hands raw pointers to the C ABI, so it refuses tensors the
+    library would misread: a transposed or column-sliced view, a host
+    tensor, a tensor of another element type (checks only, no arithmetic)."""
+    import torch
+    desc = fg.BShuf()
+    desc.mode, desc.N, desc.K = fg.FG_FP8_TENSOR, 256, 128
+    pb = fg.PreshuffledB(desc, torch.empty(0, dtype=torch.uint8), None)
+    A = torch.zeros(128, 4, dtype=torch.uint8)
+    with pytest.raises(ValueError, match="contiguous"):
+        fg.gemm(A.t(), pb)                       # transposed [4][128] view
+    with pytest.raises(ValueError, match="contiguous"):
+        fg.gemm(torch.zeros(4, 256, dtype=torch.uint8)[:, :128], pb)
+    with pytest.raises(ValueError, match="CUDA"):
+        fg.gemm(torch.zeros(4, 128, dtype=torch.uint8), pb)
+    with pytest.raises(ValueError, match="contiguous"):
+        fg.preshuffle_b("fp8_tensor", torch.zeros(128, 256, dtype=torch.uint8).t())
+    with pytest.raises(ValueError, match="CUDA"):
+        fg.preshuffle_b("fp8_tensor", torch.zeros(256, 128, dtype=torch.uint8))
+    with pytest.raises(ValueError, match="Y"):
+        fg.gemm_noalloc(torch.zeros(4, 128, dtype=torch.uint8), pb, None)
+    with pytest.raises(ValueError, match="contiguous"):
+        fg.gemm_splitk_reduce(torch.zeros(8, 4).t(), 1, 4, 8)

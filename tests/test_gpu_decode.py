@@ -181,7 +181,7 @@ def test_all_ones_is_exact(mode):
 DECODE = [(m, n) for m, n in inputs.DECODE_SHAPES]
 
 
-@pytest.mark.parametrize("mode", ["fp8_tensor", "fp8_block128", "mxfp8", "mxfp4", "mxfp8_b32", "mxfp4_fp8a"])
+@pytest.mark.parametrize("mode", MODES)
 @pytest.mark.parametrize("M,N", DECODE)
 def test_decode_workload_parity(mode, M, N):
     """The pages' decode shapes (K=7168) in the dispatch-chosen configuration,
@@ -195,6 +195,42 @@ def test_decode_workload_parity(mode, M, N):
         parity.assert_ws_close(c.partials(S), c.ref_ws(S), f"{mode} {M}x{N} ws")
     y = y_to_f64(c.gemm())
     parity.assert_y_close(y, ref, f"{mode} {M}x{N}")
+
+
+def test_c1_split4_parity():
+    """The first of the pages' decode configurations as stated: fp8
+    per-tensor, M=1, N=2048, K=7168 with split_k fixed at 4 (not the
+    dispatch's choice): the fp32 partials of the four splits at the
+    workspace bound, and every output."""
+    A, B, a_s, b_s = inputs.workload_operands("fp8_tensor_decode_m1_n2048_k7168_split4", 0)
+    c = Case("fp8_tensor", A, B, a_s, b_s)
+    assert fg.gemm_plan("fp8_tensor", 1, 2048, 7168, split_k=4)["split_k"] == 4
+    parity.assert_ws_close(c.partials(4), c.ref_ws(4), "C1 ws S=4")
+    parity.assert_y_close(y_to_f64(c.gemm(split_k=4)), c.ref(), "C1 y S=4")
+    assert fg.get_error() == fg.FG_OK
+
+
+@pytest.mark.parametrize("mode", MODES)
+def test_two_pass_split16_matches_oracle(mode):
+    """Splits above the cluster limit take the workspace + reduce-kernel
+    path: 16 splits (ragged token tile, three weight tiles), the partials at
+    the workspace bound and every output against the oracle."""
+    M, N, K = 5, 384, 4096
+    c = Case(mode, *inputs.operands(mode, M, N, K, 910, 911, 912))
+    assert fg.gemm_workspace_size(mode, M, N, K, 16) == 16 * M * N * 4
+    parity.assert_ws_close(c.partials(16), c.ref_ws(16), f"{mode} ws S=16")
+    parity.assert_y_close(y_to_f64(c.gemm(split_k=16)), c.ref(), f"{mode} y S=16")
+    assert fg.get_error() == fg.FG_OK
+
+
+@pytest.mark.parametrize("mode", ["fp8_tensor", "fp8_block128", "mxfp4"])
+def test_two_pass_split16_workload_shape(mode):
+    """Split 16 at a decode shape of the pages (M=16, N=2048, K=7168):
+    every output against the oracle."""
+    M, N, K = 16, 2048, 7168
+    c = Case(mode, *inputs.operands(mode, M, N, K, 920, 921, 922))
+    parity.assert_y_close(y_to_f64(c.gemm(split_k=16)), c.ref(), f"{mode} {M}x{N}x{K} S=16")
+    assert fg.get_error() == fg.FG_OK
 
 
 # -------------------------------------------------------- negative controls
@@ -248,6 +284,29 @@ def test_error_paths_on_device():
     # M == 0: no-op
     fg.gemm(c.dA[:0], c.pb, c.da_s, Y=Y[:0])
     parity.assert_y_close(y_to_f64(c.gemm()), c.ref(), "after errors")
+
+
+def test_binding_rejects_views_that_would_be_misread():
+    """A transposed A, a column slice of a wider buffer, activations of the
+    wrong element type, and a Y of the wrong shape are refused by the
+    binding with ValueError before anything is launched."""
+    M, N, K = 4, 256, 1024
+    c = Case("fp8_tensor", *inputs.operands("fp8_tensor", M, N, K, 64, 65, 66))
+    Y = torch.zeros((M, N), dtype=torch.bfloat16, device="cuda")
+    with pytest.raises(ValueError, match="contiguous"):
+        fg.gemm(c.dA.t().contiguous().t(), c.pb, c.da_s, Y=Y)      # same shape, column-major
+    with pytest.raises(ValueError, match="contiguous"):
+        wide = torch.zeros((M, 2 * K), dtype=torch.uint8, device="cuda")
+        fg.gemm(wide[:, :K], c.pb, c.da_s, Y=Y)
+    with pytest.raises(ValueError, match="dtype"):
+        fg.gemm(c.dA.float(), c.pb, c.da_s, Y=Y)
+    with pytest.raises(ValueError, match="shape"):
+        fg.gemm(c.dA, c.pb, c.da_s, Y=torch.zeros((M, N // 2), dtype=torch.bfloat16, device="cuda"))
+    with pytest.raises(ValueError, match="dtype"):
+        fg.gemm(c.dA, c.pb, c.da_s.double(), Y=Y)
+    torch.cuda.synchronize()
+    assert not Y.any()
+    parity.assert_y_close(y_to_f64(fg.gemm(c.dA, c.pb, c.da_s, Y=Y)), c.ref(), "after refusals")
 
 
 def test_bounded_wait_reports_timeout_and_context_survives():

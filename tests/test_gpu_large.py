@@ -57,6 +57,7 @@ def test_large_identity_is_bit_exact(mode):
     ("mxfp8", 4096, 16384, 7168, "mx_mxfp8_mxfp4_n16384_k7168", 2),
     ("mxfp4", 4096, 16384, 7168, "mx_mxfp8_mxfp4_n16384_k7168", 5),
     ("mxfp4_fp8a", 4096, 16384, 7168, "mx_fp8a_fp4w_n16384_k7168", 2),
+    ("mxfp8_b32", 4096, 16384, 7168, "mx_mxfp8_b32_n16384_k7168", 2),
 ])
 def test_large_workload_parity_sampled_rows(mode, M, N, K, name, idx):
     A, B, a_s, b_s = inputs.workload_operands(name, idx)

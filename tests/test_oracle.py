@@ -82,6 +82,65 @@ def test_bf16_decode_matches_torch_all_patterns():
     assert np.array_equal(ref[~nan], got[~nan])
 
 
+# --------------------------------------------------------- output rounding
+
+def _bf16_round_cases():
+    """fp32 values that a wrong bf16 rounding (truncation, ties away from zero
+    or to odd, a lost sign, a flushed subnormal, no overflow to inf, a NaN
+    turned into inf) gets wrong: random values over every binade, the exact
+    midpoint between every pair of neighbouring finite bf16 values (both
+    signs), the values one fp32 ulp either side of those midpoints, +-0,
+    fp32 subnormals, the overflow boundary, +-inf and NaNs."""
+    g = np.random.default_rng(77)
+    rand_bits = g.integers(0, 2 ** 32, 200_000, dtype=np.uint64).astype(np.uint32)
+    # every finite non-negative bf16 pattern b and its successor b + 1:
+    # their midpoint is b's fp32 pattern + 0x8000 (exact in fp32)
+    b = np.arange(0x0000, 0x7F7F, dtype=np.uint32)
+    mid = (b << 16) + 0x8000
+    near = np.concatenate([mid - 1, mid, mid + 1])
+    special = np.array([0x00000000, 0x80000000, 0x00000001, 0x807FFFFF, 0x00400000, 0x00008000,
+                        0x7F7F7FFF, 0x7F7F8000, 0x7F7FFFFF, 0xFF7F8000, 0x7F800000, 0xFF800000,
+                        0x7FC00000, 0x7F800001, 0xFFFFFFFF, 0x7FBFFFFF], np.uint32)
+    bits = np.concatenate([rand_bits, near, near | 0x80000000, special]).astype(np.uint32)
+    return bits.view(np.float32)
+
+
+def test_round_bf16_matches_torch_and_ml_dtypes():
+    """orc_round_bf16 (fp64 -> fp32 -> bf16, round to nearest even) against
+    two independent casts on fp32-exact inputs, including every tie."""
+    import torch
+    x32 = _bf16_round_cases()
+    got = oracle.round_bf16(x32.astype(np.float64))
+    ref_t = torch.from_numpy(x32.copy()).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    with np.errstate(invalid="ignore"):
+        ref_m = x32.astype(ml.bfloat16).view(np.uint16)
+    nan = np.isnan(x32)
+    # NaN payloads may differ between implementations; a NaN must stay a NaN
+    assert np.all((got[nan] & 0x7F80) == 0x7F80) and np.all((got[nan] & 0x007F) != 0)
+    assert np.array_equal(got[~nan], ref_t[~nan])
+    assert np.array_equal(got[~nan], ref_m[~nan])
+    # ties go to the even bf16 code: 1 + 2^-8 lies halfway between 1 and 1 + 2^-7
+    assert oracle.round_bf16(np.array([1.0 + 2.0 ** -8]))[0] == 0x3F80
+    assert oracle.round_bf16(np.array([1.0 + 3 * 2.0 ** -8]))[0] == 0x3F82
+    assert oracle.round_bf16(np.array([-(1.0 + 2.0 ** -8)]))[0] == 0xBF80
+
+
+def test_round_bf16_rounds_fp64_through_fp32():
+    """The oracle's fp64 results are rounded first to fp32 (the kernels'
+    accumulator type) and then to bf16, each step to nearest even -- the
+    same as an independent library taking the same two steps."""
+    import torch
+    g = np.random.default_rng(78)
+    x = g.standard_normal(100_000) * np.exp2(g.integers(-30, 30, 100_000))
+    got = oracle.round_bf16(x)
+    ref = torch.from_numpy(x).to(torch.float32).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    assert np.array_equal(got, ref)
+    # a value just above a bf16 midpoint in fp64 that lands exactly on the
+    # midpoint in fp32 is decided by the fp32 tie rule (even), as on the GPU
+    v = 1.0 + 2.0 ** -8 + 2.0 ** -40
+    assert oracle.round_bf16(np.array([v]))[0] == 0x3F80
+
+
 # ------------------------------------------------- independent brute force
 
 def _frac_values(mode, X, S, rows, K, is_b):
