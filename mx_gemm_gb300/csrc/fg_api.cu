@@ -183,6 +183,17 @@ int large_tile_m(int mode, int64_t M, int64_t N) {
   return wide_tiles >= sm_count() ? 256 : 128;
 }
 
+// Large-M MX on CTA pairs (256 x 256 tiles, two SMs per tile): built and
+// correct, but measured 2-6 % slower than the one-CTA 128 x 256 form at the
+// pages' M = 4096 shapes (both are bound by the L2 -> SM stream, see the pair
+// kernel's file), so the dispatch keeps the one-CTA form.  FG_LARGE_PAIR=1
+// selects the pair form (when the device can hold clusters of two).
+bool large_pair(int mode, int64_t /*M*/, int64_t /*N*/) {
+  if (!is_mx(mode)) return false;
+  const char* ov = getenv("FG_LARGE_PAIR");
+  return ov && strcmp(ov, "1") == 0 && pair_max_clusters() > 0;
+}
+
 fg_status make_plan(int mode, int64_t M, int64_t N, int64_t K, int split_k, fg_plan* out) {
   memset(out, 0, sizeof *out);
   const int64_t Kb = row_bytes(mode, K);
@@ -195,9 +206,19 @@ fg_status make_plan(int mode, int64_t M, int64_t N, int64_t K, int split_k, fg_p
   if (large) {
     out->path = 1;
     out->split_k = 1;
-    out->tile_m = large_tile_m(mode, M, N);
     out->tile_n = 256;
     out->stage_slabs = 1;
+    if (large_pair(mode, M, N)) {
+      out->tile_m = 256;
+      out->stages = 6;
+      const int64_t tiles = ((M + 255) / 256) * ((N + 255) / 256);
+      const int64_t clusters = pair_max_clusters();
+      out->ctas = static_cast<int32_t>(2 * (tiles < clusters ? tiles : clusters));
+      snprintf(out->name, sizeof out->name, "fg_large_sm103a_%s_m%lld_n%lld_k%lld_pair256x256", mode_name(mode),
+               (long long)M, (long long)N, (long long)K);
+      return FG_OK;
+    }
+    out->tile_m = large_tile_m(mode, M, N);
     out->stages = out->tile_m == 256 ? 3 : 4;
     const int64_t tiles = ((M + out->tile_m - 1) / out->tile_m) * (N / 256 + (N % 256 ? 1 : 0));
     out->ctas = static_cast<int32_t>(tiles < sm_count() ? tiles : sm_count());
@@ -315,6 +336,25 @@ fg_status make_tmap(CUtensorMap* map, const void* base, int64_t rows, int64_t rb
                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS) return fail(FG_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d)", static_cast<int>(r));
+  return FG_OK;
+}
+
+// Plain (unswizzled) 2-D map over `rows` rows of `rbytes` bytes (a multiple
+// of 8, at most 2048) in 8-byte elements, with a box of box_rows whole rows:
+// the weight image as 2 KiB rows (a 16 KiB slab is 8 of them) or a scale
+// image as 512-byte atoms.  Long rows keep the number of row requests per
+// copy small.  Rows past the end read as zero.
+fg_status make_tmap_rows(CUtensorMap* map, const void* base, int64_t rows, uint32_t rbytes, uint32_t box_rows) {
+  auto fn = encode_fn();
+  if (!fn) return fail(FG_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
+  cuuint64_t dims[2] = {static_cast<cuuint64_t>(rbytes / 8), static_cast<cuuint64_t>(rows)};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(rbytes)};
+  cuuint32_t box[2] = {rbytes / 8, box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_INT64, 2, const_cast<void*>(base), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return fail(FG_ERR_CUDA, "cuTensorMapEncodeTiled (rows) failed (%d)", static_cast<int>(r));
   return FG_OK;
 }
 
@@ -575,6 +615,41 @@ fg_status fg_gemm(const void* A, const void* a_scales, int64_t M, const fg_bshuf
   memset(&tmap_b, 0, sizeof tmap_b);
   if (mode == FG_MXFP4_FP8A && (s = make_tmap_fp4w(&tmap_b, b->data, N, K)) != FG_OK) return s;
   cudaError_t e;
+  if (plan.path == 1 && mx && plan.tile_m == 256) {
+    // CTA-pair form: every operand arrives by tensor copy (their byte counts
+    // complete on the even CTA's barriers)
+    if ((s = make_tmap(&tmap, A, M, rb, 128)) != FG_OK) return s;
+    const int64_t KBb = row_bytes(mode, K) / 128;
+    if (mode != FG_MXFP4_FP8A && (s = make_tmap_rows(&tmap_b, b->data, (N / 128) * KBb * 8, 2048, 8)) != FG_OK)
+      return s;
+    const uint64_t asf_bytes = large_mx_workspace(mode, M, K);
+    CUtensorMap tmap_asf, tmap_bsf;
+    const uint32_t box = pair_sf_box_rows(mode);
+    if ((s = make_tmap_rows(&tmap_asf, workspace, static_cast<int64_t>(asf_bytes / 512), 512, box)) != FG_OK) return s;
+    if ((s = make_tmap_rows(&tmap_bsf, b->sf, static_cast<int64_t>(b->sf_bytes / 512), 512, box)) != FG_OK) return s;
+    LargeParams p;
+    memset(&p, 0, sizeof p);
+    p.b_img = static_cast<const uint8_t*>(b->data);
+    p.b_sf = static_cast<const uint8_t*>(b->sf);
+    p.a_scales = a_scales;
+    p.y = static_cast<__nv_bfloat16*>(Y);
+    p.err = err;
+    p.timeout_ns = g_timeout_ns.load();
+    p.M = static_cast<int>(M);
+    p.N = static_cast<int>(N);
+    p.K = static_cast<int>(K);
+    p.KB = static_cast<int>(KBb);
+    p.tiles_m = static_cast<int>((M + 255) / 256);
+    p.tiles_n = static_cast<int>((N + 255) / 256);
+    p.debug_stall = (flags & FG_FLAG_DEBUG_STALL) ? 1 : 0;
+    e = launch_relayout_sf_rows(mode, static_cast<const uint8_t*>(a_scales), static_cast<uint8_t*>(workspace), M, K,
+                                st);
+    if (e != cudaSuccess) return cuda_fail(e, "A scale relayout launch");
+    p.a_sf = static_cast<const uint8_t*>(workspace);
+    e = launch_large_pair(mode, tmap, tmap_b, tmap_asf, tmap_bsf, p, plan.ctas, st);
+    if (e != cudaSuccess) return cuda_fail(e, "large-M pair kernel launch");
+    return FG_OK;
+  }
   if (plan.path == 1) {
     if ((s = make_tmap(&tmap, A, M, rb, 128)) != FG_OK) return s;
     LargeParams p;

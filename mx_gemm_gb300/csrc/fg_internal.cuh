@@ -90,6 +90,17 @@ cudaError_t launch_decode(const DecodeConfig& cfg, const CUtensorMap& tmap_a, co
                           const DecodeParams& p, dim3 grid, cudaStream_t stream);
 
 bool large_supported(int mode);
+// CTA-pair form of the large-M MX kernel (256 x 256 tiles on two SMs):
+// clusters of two that fit on the device at once (0 if unknown), the atom
+// count of one scale box (the atoms of one 128-row block and slab), and the
+// launch.  tmap_b: the weight image as 2 KiB rows of 8-byte elements (box 8
+// rows) or, for kMXFP4FP8A, the 3-D map above; tmap_asf / tmap_bsf: the A and
+// weight scale images as 512-byte rows (one atom each).
+int pair_max_clusters();
+uint32_t pair_sf_box_rows(int mode);
+cudaError_t launch_large_pair(int mode, const CUtensorMap& tmap_a, const CUtensorMap& tmap_b,
+                              const CUtensorMap& tmap_asf, const CUtensorMap& tmap_bsf, const LargeParams& p,
+                              int ctas, cudaStream_t stream);
 cudaError_t launch_large(int mode, const CUtensorMap& tmap_a, const CUtensorMap& tmap_b, const LargeParams& p,
                          int ctas, cudaStream_t stream);
 

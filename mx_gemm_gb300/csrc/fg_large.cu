@@ -29,6 +29,7 @@
 
 #include "fg_internal.cuh"
 #include "fg_ptx.cuh"
+#include "fg_tiles.cuh"
 
 namespace fg {
 
@@ -43,29 +44,7 @@ constexpr int kBBytes = kBN * 128;        // 32 KiB
 constexpr int kStageBytes = kABytes + kBBytes;
 constexpr int kSmem = kStages * kStageBytes + 1024;
 constexpr int kTmemCols = 512;            // two 256-column accumulators
-constexpr int kGroupN = 16;
-
 static_assert(kSmem <= 232448, "shared memory budget");
-
-struct TileCoord {
-  int m, n;
-};
-
-__device__ __forceinline__ TileCoord tile_coord(int t, int tiles_m, int tiles_n) {
-  const int per_group = kGroupN * tiles_m;
-  const int g = t / per_group;
-  const int r = t - g * per_group;
-  const int gn = min(kGroupN, tiles_n - g * kGroupN);
-  TileCoord c;
-  c.m = r / gn;
-  c.n = g * kGroupN + (r - c.m * gn);
-  return c;
-}
-
-__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
-  const __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
-  return *reinterpret_cast<const uint32_t*>(&v);
-}
 
 // One unit of a CTA's work: K iterations [k0, k1) of tile t.
 struct Chunk {

@@ -171,3 +171,90 @@ def test_wide_tile_bounded_wait_reports_timeout(mode, monkeypatch):
         fg.set_wait_timeout_ns(4_000_000_000)
     assert fg.get_error() == fg.FG_OK
     parity.assert_y_close(y_to_f64(c.gemm()), c.ref(), f"{mode} 256x256 after timeout")
+
+
+# ------------------------------------------------------ MX on CTA pairs
+
+MX = ["mxfp8", "mxfp4", "mxfp8_b32", "mxfp4_fp8a"]
+
+
+@pytest.mark.parametrize("mode", MX)
+@pytest.mark.parametrize("M,N,K", [(33, 256, 512), (129, 384, 2048), (300, 512, 1024), (1000, 1280, 1536)])
+def test_pair_small_shapes(mode, M, N, K, monkeypatch):
+    """The CTA-pair form (256 x 256 tiles on two SMs) forced on small shapes:
+    an odd CTA whose rows of A lie past M, a weight tile whose second half
+    lies past N, several tiles per pair; every output against the oracle."""
+    monkeypatch.setenv("FG_LARGE_PAIR", "1")
+    plan = fg.gemm_plan(mode, M, N, K)
+    assert plan["path"] == 1 and plan["name"].endswith("pair256x256")
+    c = Case(mode, *inputs.operands(mode, M, N, K, 110 + M, 120 + N, 130 + K))
+    parity.assert_y_close(y_to_f64(c.gemm()), c.ref(), f"{mode} {M}x{N}x{K} pair")
+    assert fg.get_error() == fg.FG_OK
+
+
+@pytest.mark.parametrize("mode", MX)
+def test_pair_identity_is_bit_exact(mode, monkeypatch):
+    monkeypatch.setenv("FG_LARGE_PAIR", "1")
+    M, N, K = 300, 512, 1024
+    _, B, _, b_s = inputs.operands(mode, 1, N, K, 3, 4, 5)
+    A = np.zeros((M, K), np.uint8)
+    for m in range(M):
+        A[m, (3 * m + 1) % K] = 0x2 if mode == "mxfp4" else 0x38
+    if mode == "mxfp4":
+        A = inputs.pack_e2m1(A)
+    a_s = np.full((M, K // (128 if mode == "mxfp8" else 32)), 127, np.uint8)
+    c = Case(mode, A, B, a_s, b_s)
+    ref = c.ref()
+    assert np.array_equal(y_to_f64(c.gemm()), parity.bf16_bits_to_f64(oracle.round_bf16(ref)))
+
+
+@pytest.mark.parametrize("mode", MX)
+def test_pair_and_single_cta_forms_agree(mode, monkeypatch):
+    """Both large-M MX forms accumulate every output over the same K order
+    with MMAs of the same K: the same results within the output bound, and a
+    pair tile count that leaves some pairs a second tile."""
+    M, N, K = 2304, 2560, 1024        # 9 x 10 pair tiles on 76 pairs
+    c = Case(mode, *inputs.operands(mode, M, N, K, 141, 142, 143))
+    monkeypatch.setenv("FG_LARGE_PAIR", "1")
+    y_pair = c.gemm()
+    monkeypatch.setenv("FG_LARGE_PAIR", "0")
+    y_one = c.gemm()
+    parity.assert_y_close(y_to_f64(y_pair), y_to_f64(y_one), f"{mode} pair vs one-CTA")
+    rows = inputs.sample_rows(M, n=64)
+    parity.assert_y_close(y_to_f64(y_pair[torch.from_numpy(rows).cuda()]), c.ref(rows=rows), f"{mode} pair")
+    assert fg.get_error() == fg.FG_OK
+
+
+@pytest.mark.parametrize("mode,name,idx", [("mxfp4", "mx_mxfp8_mxfp4_n16384_k7168", 5),
+                                           ("mxfp8", "mx_mxfp8_mxfp4_n16384_k7168", 2)])
+def test_pair_workload_parity_sampled_rows(mode, name, idx, monkeypatch):
+    """The pair form at the pages' MX shape (4096 x 16384 x 7168): 256 seeded
+    rows against the oracle."""
+    monkeypatch.setenv("FG_LARGE_PAIR", "1")
+    A, B, a_s, b_s = inputs.workload_operands(name, idx)
+    c = Case(mode, A, B, a_s, b_s)
+    assert fg.gemm_plan(mode, 4096, 16384, 7168)["name"].endswith("pair256x256")
+    Y = c.gemm()
+    rows = inputs.sample_rows(4096)
+    parity.assert_y_close(y_to_f64(Y[torch.from_numpy(rows).cuda()]), c.ref(rows=rows), f"{mode} pair workload")
+    assert fg.get_error() == fg.FG_OK
+
+
+@pytest.mark.parametrize("mode", ["mxfp8", "mxfp4"])
+def test_pair_bounded_wait_reports_timeout(mode, monkeypatch):
+    """The even CTA's MMA issuer waits on a barrier nothing arrives at: both
+    CTAs' waits run out, the even CTA completes every stage either producer
+    started, the pair releases its memory and returns, the host reads
+    FG_ERR_TIMEOUT, and a normal call afterwards is correct."""
+    monkeypatch.setenv("FG_LARGE_PAIR", "1")
+    M, N, K = 600, 512, 2048
+    c = Case(mode, *inputs.operands(mode, M, N, K, 87, 88, 89))
+    assert fg.get_error() == fg.FG_OK
+    fg.set_wait_timeout_ns(20_000_000)
+    try:
+        c.gemm(flags=fg.FG_FLAG_DEBUG_STALL)
+        assert fg.get_error() == fg.FG_ERR_TIMEOUT
+    finally:
+        fg.set_wait_timeout_ns(4_000_000_000)
+    assert fg.get_error() == fg.FG_OK
+    parity.assert_y_close(y_to_f64(c.gemm()), c.ref(), f"{mode} pair after timeout")
