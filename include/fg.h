@@ -273,9 +273,9 @@ FG_API fg_status fg_gemm_splitk_reduce(const float* ws, int split_k, int64_t M, 
  *  - All calls share the one array and it keeps the last call's contents.
  *    Nothing in it has to start at zero (every split writes its whole
  *    partial before the reduce reads it, every large-M MX call rewrites its
- *    whole A scale image, a stream-K flag matches only the launch that wrote
- *    it), but two calls that overlap on the GPU (e.g. on two streams) race on
- *    it: serialise them.
+ *    whole A scale image, a partial's flag matches only the launch that
+ *    wrote it and is cleared once read), but two calls that overlap on the
+ *    GPU (e.g. on two streams) race on it: serialise them.
  * Errors: as fg_gemm.
  */
 FG_API fg_status fg_gemm_noalloc(const void* A, const void* a_scales, int64_t M, const fg_bshuf* b, int mode,

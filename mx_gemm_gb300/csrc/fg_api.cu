@@ -149,6 +149,7 @@ struct TableRow {
 // split_k other than the row's keeps the heuristic's pipeline.
 const TableRow kTable[] = {
     {FG_FP8_TENSOR, 1, 2048, 7168, 8, 1, 6},     {FG_FP8_TENSOR, 16, 2048, 7168, 8, 1, 6},
+    {FG_FP8_TENSOR, 1, 2048, 7168, 4, 2, 5},  // an explicit split of 4 at this shape
     {FG_FP8_TENSOR, 1, 16384, 7168, 2, 2, 3},    {FG_FP8_TENSOR, 16, 16384, 7168, 1, 2, 5},
     {FG_FP8_BLOCK128, 1, 2048, 7168, 8, 1, 4},   {FG_FP8_BLOCK128, 16, 2048, 7168, 8, 1, 4},
     {FG_FP8_BLOCK128, 1, 16384, 7168, 2, 1, 4},  {FG_FP8_BLOCK128, 16, 16384, 7168, 2, 1, 4},
@@ -298,8 +299,10 @@ uint64_t large_streamk_plan(int mode, int64_t tiles, int64_t KB, int ctas, Large
   return large_streamk_bytes(ctas, wide);
 }
 
-// A 64-bit tag per launch: a stream-K flag matches only the launch that
-// wrote it (workspace contents from earlier calls never do).
+// A 64-bit tag per call: a partial's flag matches only the launch that wrote
+// it (workspace contents from earlier calls never do), and the CTA that
+// consumes a partial clears its flag, so a replay of a captured launch (which
+// reuses its tag) waits for its own partial.
 uint64_t next_epoch() {
   static std::atomic<uint64_t> counter{0};
   static const uint64_t salt = (static_cast<uint64_t>(reinterpret_cast<uintptr_t>(&counter)) * 0x9E3779B97F4A7C15ull) ^
@@ -553,7 +556,9 @@ fg_status fg_gemm_workspace_size(int mode, int64_t M, int64_t N, int64_t K, int 
   fg_plan plan;
   fg_status s = fg_gemm_plan(mode, M, N, K, split_k, &plan);
   if (s != FG_OK) return s;
-  if (plan.path == 1) {
+  if (M == 0) {
+    *bytes = 0;
+  } else if (plan.path == 1) {
     const int64_t tiles = ((M + plan.tile_m - 1) / plan.tile_m) * (N / 256 + (N % 256 ? 1 : 0));
     *bytes = is_mx(mode) ? large_mx_workspace(mode, M, K)
                          : large_streamk_plan(mode, tiles, row_bytes(mode, K) / 128, plan.ctas, nullptr,

@@ -268,6 +268,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
           }
         }
+        if (finish && have_peer) {
+          // consumed: clear the flag, so that a replay of this launch (same
+          // epoch, e.g. in a CUDA graph) waits for the partial it writes
+          __syncwarp();
+          if (lane == 0) p.sk_flag[(blockIdx.x + 1) * 4 + qd] = 0;
+        }
       }
       tc_fence_before();
       __syncwarp();
@@ -531,6 +537,11 @@ __global__ void __launch_bounds__(kWideThreads, 1)
         __threadfence();
         __syncwarp();
         if (lane == 0) st_release_u64(p.sk_flag + blockIdx.x * 8 + ew, p.epoch);
+      } else if (finish && have_peer) {
+        // consumed: clear the flag, so that a replay of this launch (same
+        // epoch, e.g. in a CUDA graph) waits for the partial it writes
+        __syncwarp();
+        if (lane == 0) p.sk_flag[(blockIdx.x + 1) * 8 + ew] = 0;
       }
     }
   }

@@ -91,8 +91,10 @@ def test_plan_heuristic_and_table(fg):
     assert p["split_k"] == 1 and (p["stage_slabs"], p["stages"]) == (2, 5) and p["from_table"]
     p = fg.gemm_plan("fp8_tensor", 8, 4096, 4096)          # heuristic: >= 1.5 CTAs per SM
     assert not p["from_table"] and p["ctas"] >= 1.5 * 148
-    p = fg.gemm_plan("fp8_tensor", 1, 2048, 7168, split_k=4)   # another split than the row's
-    assert p["split_k"] == 4 and not p["from_table"] and (p["stage_slabs"], p["stages"]) == (1, 4)
+    p = fg.gemm_plan("fp8_tensor", 1, 2048, 7168, split_k=4)   # the row for an explicit split of 4
+    assert p["split_k"] == 4 and p["from_table"] and (p["stage_slabs"], p["stages"]) == (2, 5)
+    p = fg.gemm_plan("fp8_tensor", 1, 2048, 7168, split_k=2)   # a split no row has: the heuristic pipeline
+    assert p["split_k"] == 2 and not p["from_table"] and (p["stage_slabs"], p["stages"]) == (1, 4)
     p = fg.gemm_plan("fp8_tensor", 1, 2048, 7168, split_k=8)   # the row's own split
     assert p["from_table"] and (p["stage_slabs"], p["stages"]) == (1, 6)
     assert "sm103a" in p["name"] and "n2048" in p["name"] and "k7168" in p["name"]

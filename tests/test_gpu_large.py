@@ -258,3 +258,35 @@ def test_pair_bounded_wait_reports_timeout(mode, monkeypatch):
         fg.set_wait_timeout_ns(4_000_000_000)
     assert fg.get_error() == fg.FG_OK
     parity.assert_y_close(y_to_f64(c.gemm()), c.ref(), f"{mode} pair after timeout")
+
+
+@pytest.mark.parametrize("tile", ["128", "256"])
+def test_streamk_graph_replay_sees_new_inputs(tile, monkeypatch):
+    """A stream-K call captured in a CUDA graph and replayed twice with A
+    overwritten in between: the second replay must use its own partials, not
+    those the first replay published under the same launch tag."""
+    monkeypatch.setenv("FG_LARGE_TILE", tile)
+    mode = "fp8_tensor"
+    M, N, K = (2560, 2048, 1024) if tile == "128" else (6144, 6144, 1024)
+    c = Case(mode, *inputs.operands(mode, M, N, K, 370, 371, 372))
+    A2, _, _, _ = inputs.operands(mode, M, N, K, 373, 371, 372)
+    need = fg.gemm_workspace_size(mode, M, N, K)
+    assert need > 0
+    ws = torch.empty(need // 4, dtype=torch.float32, device="cuda")
+    Y = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
+    A = c.dA.clone()
+    g = torch.cuda.CUDAGraph()
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.graph(g, stream=s):
+        fg.gemm(A, c.pb, c.da_s, Y=Y, workspace=ws)
+    torch.cuda.synchronize()
+    g.replay()
+    torch.cuda.synchronize()
+    A.copy_(torch.from_numpy(A2).cuda())
+    g.replay()
+    torch.cuda.synchronize()
+    rows = inputs.sample_rows(M, n=64)
+    c2 = Case(mode, A2, c.B, c.a_s, c.b_s)
+    parity.assert_y_close(y_to_f64(Y[torch.from_numpy(rows).cuda()]), c2.ref(rows=rows), f"stream-K {tile} replay")
+    assert fg.get_error() == fg.FG_OK
