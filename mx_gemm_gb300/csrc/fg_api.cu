@@ -200,7 +200,8 @@ fg_status make_plan(int mode, int64_t M, int64_t N, int64_t K, int split_k, fg_p
   const int64_t Kb = row_bytes(mode, K);
   const int64_t KB = Kb / 128;
   const int64_t tiles_n = N / 128;
-  const int64_t tiles_m = (M + 15) / 16;
+  const int tok = M > 16 ? 32 : 16;
+  const int64_t tiles_m = (M + tok - 1) / tok;
   // The large-M kernel has no K split; an explicit split_k > 1 keeps any M on
   // the split-K kernel (which covers M in 16-row tiles).
   const bool large = M > decode_row_limit() && large_supported(mode) && split_k <= 1;
@@ -229,6 +230,8 @@ fg_status make_plan(int mode, int64_t M, int64_t N, int64_t K, int split_k, fg_p
   }
   int split = split_k, sps = 1, stages = 4;
   bool from_table = false;
+  // 17..32 tokens (and more, where no large-M form exists) take 32-token
+  // tiles: the weights stream once per 32 tokens instead of per 16
   for (const TableRow& r : kTable) {
     if (r.mode == mode && r.N == N && r.K == K && M <= r.m_max && (r.m_max == 1 ? M == 1 : M > 1) &&
         (split == 0 || split == r.split)) {
@@ -253,8 +256,9 @@ fg_status make_plan(int mode, int64_t M, int64_t N, int64_t K, int split_k, fg_p
   if (const char* ov = getenv("FG_DECODE_CONFIG")) {
     int a = 0, b = 0;
     char tail = 0;
-    if (sscanf(ov, "%d,%d%c", &a, &b, &tail) != 2 || !decode_config_supported(DecodeConfig{mode, a, b}))
-      return fail(FG_ERR_INVALID_ARG, "FG_DECODE_CONFIG=\"%s\" is not an instantiated <slabs>,<stages> pair", ov);
+    if (sscanf(ov, "%d,%d%c", &a, &b, &tail) != 2 || !decode_config_supported(DecodeConfig{mode, a, b, tok}))
+      return fail(FG_ERR_INVALID_ARG, "FG_DECODE_CONFIG=\"%s\" is not an instantiated <slabs>,<stages> pair%s", ov,
+                  tok == 32 ? " for 32-token tiles (one slab per stage)" : "");
     sps = a;
     stages = b;
   }
@@ -264,7 +268,7 @@ fg_status make_plan(int mode, int64_t M, int64_t N, int64_t K, int split_k, fg_p
                 (long long)K);
   out->path = 0;
   out->split_k = split;
-  out->tile_m = 16;
+  out->tile_m = tok;
   out->tile_n = 128;
   out->stage_slabs = sps;
   out->stages = stages;
@@ -697,7 +701,7 @@ fg_status fg_gemm(const void* A, const void* a_scales, int64_t M, const fg_bshuf
     if (e != cudaSuccess) return cuda_fail(e, "large-M kernel launch");
     return FG_OK;
   }
-  if ((s = make_tmap(&tmap, A, M, rb, 16)) != FG_OK) return s;
+  if ((s = make_tmap(&tmap, A, M, rb, static_cast<uint32_t>(plan.tile_m))) != FG_OK) return s;
   DecodeParams p;
   memset(&p, 0, sizeof p);
   p.b_img = static_cast<const uint8_t*>(b->data);
@@ -715,9 +719,10 @@ fg_status fg_gemm(const void* A, const void* a_scales, int64_t M, const fg_bshuf
   p.split = split;
   p.fused_reduce = fused ? 1 : 0;
   p.debug_stall = (flags & FG_FLAG_DEBUG_STALL) ? 1 : 0;
-  DecodeConfig cfg{mode, plan.stage_slabs, plan.stages};
+  DecodeConfig cfg{mode, plan.stage_slabs, plan.stages, plan.tile_m};
   if (!decode_config_supported(cfg)) return fail(FG_ERR_INVALID_ARG, "no kernel for config %s", plan.name);
-  dim3 grid(static_cast<unsigned>(N / 128), static_cast<unsigned>(split), static_cast<unsigned>((M + 15) / 16));
+  dim3 grid(static_cast<unsigned>(N / 128), static_cast<unsigned>(split),
+            static_cast<unsigned>((M + plan.tile_m - 1) / plan.tile_m));
   if (grid.z > 65535) return fail(FG_ERR_SHAPE, "M=%lld too large for the decode path", (long long)M);
   e = launch_decode(cfg, tmap, tmap_b, p, grid, st);
   if (e != cudaSuccess) return cuda_fail(e, "decode kernel launch");

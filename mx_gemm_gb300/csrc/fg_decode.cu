@@ -3,10 +3,11 @@
 // What's included), written for sm_103a tensor cores.
 //
 // Orientation ("swap AB"): the weight B is the MMA's M operand (128 rows of
-// N per CTA), the <= 16 token rows of A are the MMA's N operand, so one
-// tcgen05.mma is 128 x 16 x (32 bytes of K) and the fp32 accumulator lives
-// in 16 TMEM columns.  CTA (nt, s, mt) covers weight rows [128 nt, +128),
-// token rows [16 mt, +16) and split s of the K slabs.
+// N per CTA), a tile of TOK token rows of A is the MMA's N operand -- 16, or
+// 32 when there are more than 16 tokens, so that 17..32 tokens stream the
+// weights once -- so one tcgen05.mma is 128 x TOK x (32 bytes of K) and the
+// fp32 accumulator lives in TOK TMEM columns.  CTA (nt, s, mt) covers weight
+// rows [128 nt, +128), token rows [TOK mt, +TOK) and split s of the K slabs.
 //
 // Warp roles (192 threads):
 //   warp 0    producer: one bulk copy per stage for the contiguous weight
@@ -61,12 +62,13 @@
 // (base + i/32).  tcgen05.cp.32x128b.warpx4 copies a 32-row x 16-byte
 // shared-memory atom into four TMEM columns of every 32-lane quarter, which
 // gives exactly that layout for atoms whose byte 16*(i%32) + 4*(i/32) + j
-// holds row i's scale for the j-th 32-K block.  For the 16 token rows the
+// holds row i's scale for the j-th 32-K block.  For a 16-token tile the
 // MMA reads column 0 at lanes 32q + m (m < 16) of every quarter q -- which
 // the warpx4 copy fills from source rows 0-15 -- so token atoms are laid out
 // 256 bytes apart and overlap (rows 16-31 of one atom are rows 0-15 of the
-// next).  (A copy that filled the quarters from different rows gave wrong
-// token scales: quarters 1-3 are read too.)
+// next); a 32-token tile fills whole atoms, 512 bytes apart.  (A copy that
+// filled the quarters from different rows gave wrong token scales: quarters
+// 1-3 are read too.)
 #include <cuda_bf16.h>
 
 #include <cstdio>
@@ -80,22 +82,27 @@ namespace {
 
 constexpr int kThreads = 192;
 constexpr int kSlabBytes = 16384;   // 128 rows x 128 bytes
-constexpr int kTokSlabBytes = 2048; // 16 rows x 128 bytes
-constexpr int kTokRows = 16;
 // fp4 weight block of one slab: 128 rows x 64 packed bytes.  Its tensor load
 // writes kSlabBytes of shared memory and counts these bytes on the barrier.
 constexpr int kFp4SlabBytes = 8192;
 
-template <int MODE, int SPS, int STAGES>
+// TOK: token rows per CTA tile (the MMA's N): 16, or 32 for 17..32 tokens so
+// that the weights stream once
+template <int MODE, int SPS, int STAGES, int TOK>
 struct DCfg {
   static constexpr int APS = MODE == kMXFP4 ? 2 : (is_mx(MODE) ? 1 : 0);
+  static constexpr int TOK_BYTES = TOK * 128;  // one slab of the token tile
   // fp8 activations x fp4 weights: packed fp4 blocks through the spreading
   // tensor load (a 16 KiB tile per slab in shared memory, 8 KiB from HBM)
   static constexpr bool FP4W = MODE == kMXFP4FP8A;
   static constexpr int B_BYTES = SPS * kSlabBytes;
-  static constexpr int A_BYTES = SPS * kTokSlabBytes;
+  static constexpr int A_BYTES = SPS * TOK_BYTES;
   static constexpr int SFW_BYTES = SPS * APS * 512;
-  static constexpr int SFT_BYTES = APS ? SPS * APS * 256 + 256 : 0;
+  // token scale atoms: 16 tokens fill rows 0-15 of an atom, so atoms are laid
+  // 256 bytes apart and overlap (rows 16-31 of one are rows 0-15 of the next);
+  // 32 tokens fill whole 512-byte atoms
+  static constexpr int TOK_ATOM_STRIDE = TOK == 16 ? 256 : 512;
+  static constexpr int SFT_BYTES = APS ? SPS * APS * TOK_ATOM_STRIDE + (TOK == 16 ? 256 : 0) : 0;
   static constexpr int PREPASS_WARPS = 4;  // warps 2-5: arrivals on an MX stage's full barrier
   static constexpr int STAGE_RAW = B_BYTES + A_BYTES + SFW_BYTES + SFT_BYTES;
   static constexpr int STAGE_BYTES = (STAGE_RAW + 1023) / 1024 * 1024;
@@ -110,28 +117,46 @@ struct DCfg {
   // is free, and the separate release commit (a few hundred cycles of the MMA
   // pipe per stage) is left out
   static constexpr bool PF_RELEASE = PROMOTE && NBUF >= (STAGES - 1) * SPS + 1;
-  static constexpr int TMEM_NEED = PROMOTE ? NBUF * 16 : 32 + STAGES * 2 * SF_COLS;
+  static constexpr int TMEM_NEED = PROMOTE ? NBUF * TOK : 32 + STAGES * 2 * SF_COLS;
   static constexpr int TMEM_COLS =
       TMEM_NEED <= 32 ? 32 : (TMEM_NEED <= 64 ? 64 : (TMEM_NEED <= 128 ? 128 : (TMEM_NEED <= 256 ? 256 : 512)));
   static constexpr int SMEM = STAGES * STAGE_BYTES + 1024;
+  // CTAs per SM the registers must leave room for: FP8 blockscale with 32
+  // tokens folds three 32-wide register arrays per slab and would otherwise
+  // take every register, leaving no room beside it for the next launch
+  static constexpr int MIN_CTAS = (MODE == kBlock && TOK == 32) ? 2 : 1;
   static_assert(TMEM_NEED <= 512, "TMEM budget");
+  static_assert(TOK == 16 || TOK == 32, "token tile");
+  static_assert(SPS * APS * TOK <= 128, "one token scale word per pre-pass thread");
   static_assert(SMEM <= 232448, "shared memory budget");
 };
 
-// The weight is the MMA's A operand, the tokens its B operand.
+// The weight is the MMA's A operand, the tokens its B operand (N = TOK).
+template <int TOK>
 __device__ __forceinline__ uint32_t mx_idesc(int mode, int sfid) {
-  return mode == kMXFP4        ? idesc_mx(128, kTokRows, kMxf4E2M1, sfid, sfid)
-         : mode == kMXFP4FP8A ? idesc_mx_ab(128, kTokRows, kF8f6f4E2M1, kF8f6f4E4M3, sfid, sfid)
-                               : idesc_mx(128, kTokRows, kF8f6f4E4M3, sfid, sfid);
+  return mode == kMXFP4        ? idesc_mx(128, TOK, kMxf4E2M1, sfid, sfid)
+         : mode == kMXFP4FP8A ? idesc_mx_ab(128, TOK, kF8f6f4E2M1, kF8f6f4E4M3, sfid, sfid)
+                               : idesc_mx(128, TOK, kF8f6f4E4M3, sfid, sfid);
+}
+
+// A row of the accumulator (TOK fp32 columns of this thread's TMEM lane).
+template <int TOK>
+__device__ __forceinline__ void tmem_ld_tok(uint32_t taddr, uint32_t (&v)[TOK]) {
+  if constexpr (TOK == 16)
+    tmem_ld16(taddr, v);
+  else
+    tmem_ld32(taddr, v);
 }
 
 // tmap_b: fp8 x fp4 only, the weight image as [blocks][128 rows][128 codes]
 // (see the producer); unused otherwise.
-template <int MODE, int SPS, int STAGES>
-__global__ void __launch_bounds__(kThreads, 1)
+template <int MODE, int SPS, int STAGES, int TOK>
+__global__ void __launch_bounds__(kThreads, (DCfg<MODE, SPS, STAGES, TOK>::MIN_CTAS))
     decode_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_b,
                   const DecodeParams p) {
-  using C = DCfg<MODE, SPS, STAGES>;
+  using C = DCfg<MODE, SPS, STAGES, TOK>;
+  constexpr int kTokRows = TOK;
+  constexpr int kTokSlabBytes = C::TOK_BYTES;
   extern __shared__ uint8_t dsmem[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(dsmem) + 1023) & ~uintptr_t(1023));
 
@@ -318,7 +343,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int t = 0; t < nsl * C::APS; ++t) {
             tc_cp_32x128b_warpx4(tmem + sfw_col + 4 * t, sdesc_plain_rows16(smem_u32(st + C::B_BYTES + C::A_BYTES + 512 * t)));
             tc_cp_32x128b_warpx4(tmem + sft_col + 4 * t,
-                                 sdesc_plain_rows16(smem_u32(st + C::B_BYTES + C::A_BYTES + C::SFW_BYTES + 256 * t)));
+                                 sdesc_plain_rows16(smem_u32(st + C::B_BYTES + C::A_BYTES + C::SFW_BYTES +
+                                                             C::TOK_ATOM_STRIDE * t)));
           }
         }
         for (int v = 0; v < nsl; ++v) {
@@ -331,7 +357,7 @@ __global__ void __launch_bounds__(kThreads, 1)
               break;
             }
             tc_fence_after();
-            d = tmem + pb * 16;
+            d = tmem + pb * TOK;
           }
 #pragma unroll
           for (int j = 0; j < 4; ++j) {
@@ -348,11 +374,12 @@ __global__ void __launch_bounds__(kThreads, 1)
               mma_mxf8f6f4(d, adesc, bdesc, idesc_mx(128, kTokRows, 0u, (u0 + it * SPS + v) & 3, j),
                            tmem + sfw_col + 4 * v, tmem + sft_col + 4 * v, acc);
             } else if (MODE == kMXFP8B32 || MODE == kMXFP4FP8A) {
-              mma_mxf8f6f4(d, adesc, bdesc, mx_idesc(MODE, j), tmem + sfw_col + 4 * v, tmem + sft_col + 4 * v, acc);
+              mma_mxf8f6f4(d, adesc, bdesc, mx_idesc<TOK>(MODE, j), tmem + sfw_col + 4 * v, tmem + sft_col + 4 * v,
+                           acc);
             } else {
               const int t = v * 2 + (j >> 1);
-              mma_mxf4(d, adesc, bdesc, mx_idesc(MODE, 2 * (j & 1)), tmem + sfw_col + 4 * t, tmem + sft_col + 4 * t,
-                       acc);
+              mma_mxf4(d, adesc, bdesc, mx_idesc<TOK>(MODE, 2 * (j & 1)), tmem + sfw_col + 4 * t,
+                       tmem + sft_col + 4 * t, acc);
             }
           }
           if (C::PROMOTE) {
@@ -431,7 +458,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (it + 1 < niter) wv_next = tok_sf(it + 1);
         uint8_t* sft = smem + slot * C::STAGE_BYTES + C::B_BYTES + C::A_BYTES + C::SFW_BYTES;
         if (et < nsl * C::APS * kTokRows)
-          *reinterpret_cast<uint32_t*>(sft + (et / kTokRows) * 256 + (et % kTokRows) * 16) = wv;
+          *reinterpret_cast<uint32_t*>(sft + (et / kTokRows) * C::TOK_ATOM_STRIDE + (et % kTokRows) * 16) = wv;
         fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) mbar_arrive(&full_bar[slot]);
@@ -480,8 +507,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           break;
         }
         tc_fence_after();
-        uint32_t v[16];
-        tmem_ld16(trow + pb * 16, v);
+        uint32_t v[kTokRows];
+        tmem_ld_tok<TOK>(trow + pb * TOK, v);
         tmem_wait_ld();
         tc_fence_before();
         __syncwarp();
@@ -502,8 +529,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         ok = false;
       } else {
         tc_fence_after();
-        uint32_t v[16];
-        tmem_ld16(trow, v);
+        uint32_t v[kTokRows];
+        tmem_ld_tok<TOK>(trow, v);
         tmem_wait_ld();
 #pragma unroll
         for (int m = 0; m < kTokRows; ++m) acc[m] = __uint_as_float(v[m]);
@@ -526,7 +553,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         float* dst = reinterpret_cast<float*>(smem + recv_slot(owner) * C::STAGE_BYTES) +
                      ((split * RM + j) * MV) * 4;
 #pragma unroll
-        for (int v = 0; v < 4; ++v) {
+        for (int v = 0; v < kTokRows / 4; ++v) {
           if (v < MV) {
             const float4 val = make_float4(acc[4 * v], acc[4 * v + 1], acc[4 * v + 2], acc[4 * v + 3]);
             if (owner == split)
@@ -591,11 +618,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (p.fused_reduce) cluster_wait();  // phase 2: no peer stores into this CTA any more
 }
 
-template <int MODE, int SPS, int STAGES>
+template <int MODE, int SPS, int STAGES, int TOK>
 cudaError_t launch_one(const CUtensorMap& tmap_a, const CUtensorMap& tmap_b, const DecodeParams& p, dim3 grid,
                        cudaStream_t stream) {
-  using C = DCfg<MODE, SPS, STAGES>;
-  cudaError_t e = ensure_smem_attr(reinterpret_cast<const void*>(&decode_kernel<MODE, SPS, STAGES>), C::SMEM);
+  using C = DCfg<MODE, SPS, STAGES, TOK>;
+  cudaError_t e = ensure_smem_attr(reinterpret_cast<const void*>(&decode_kernel<MODE, SPS, STAGES, TOK>), C::SMEM);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = grid;
@@ -618,7 +645,7 @@ cudaError_t launch_one(const CUtensorMap& tmap_a, const CUtensorMap& tmap_b, con
   }
   cfg.attrs = attrs;
   cfg.numAttrs = na;
-  return cudaLaunchKernelEx(&cfg, decode_kernel<MODE, SPS, STAGES>, tmap_a, tmap_b, p);
+  return cudaLaunchKernelEx(&cfg, decode_kernel<MODE, SPS, STAGES, TOK>, tmap_a, tmap_b, p);
 }
 
 // Instantiated configurations: (slabs per stage, stages).
@@ -635,15 +662,23 @@ cudaError_t launch_one(const CUtensorMap& tmap_a, const CUtensorMap& tmap_b, con
 
 bool decode_config_supported(const DecodeConfig& c) {
   if (c.mode < kBF16 || c.mode > kMXFP4FP8A) return false;
+  if (c.tok == 32) return c.sps == 1 && (c.stages == 4 || c.stages == 5 || c.stages == 6 || c.stages == 8);
+  if (c.tok != 16) return false;
   return (c.sps == 1 && (c.stages == 4 || c.stages == 5 || c.stages == 6 || c.stages == 8)) ||
          (c.sps == 2 && (c.stages == 3 || c.stages == 5)) || (c.sps == 4 && c.stages == 2);
 }
 
 cudaError_t launch_decode(const DecodeConfig& c, const CUtensorMap& tmap_a, const CUtensorMap& tmap_b,
                           const DecodeParams& p, dim3 grid, cudaStream_t stream) {
-#define FG_TRY(MODE_, SPS_, ST_)                                 \
-  if (c.mode == MODE_ && c.sps == SPS_ && c.stages == ST_)       \
-    return launch_one<MODE_, SPS_, ST_>(tmap_a, tmap_b, p, grid, stream);
+  // 32-token tiles: the one-slab-per-stage pipelines only
+#define FG_TRY(MODE_, SPS_, ST_)                                                   \
+  if (c.mode == MODE_ && c.sps == SPS_ && c.stages == ST_) {                       \
+    if constexpr (SPS_ == 1) {                                                     \
+      if (c.tok == 32) return launch_one<MODE_, SPS_, ST_, 32>(tmap_a, tmap_b, p, grid, stream); \
+    }                                                                              \
+    if (c.tok != 16) return cudaErrorInvalidValue;                                 \
+    return launch_one<MODE_, SPS_, ST_, 16>(tmap_a, tmap_b, p, grid, stream);      \
+  }
   FG_DECODE_CONFIGS(FG_TRY, kBF16)
   FG_DECODE_CONFIGS(FG_TRY, kTensor)
   FG_DECODE_CONFIGS(FG_TRY, kBlock)

@@ -24,7 +24,7 @@ inline int64_t b_row_bytes(int mode, int64_t K) { return mode == kMXFP4FP8A ? K 
 inline int sf_atoms_per_slab(int mode) { return mode == kMXFP4 ? 2 : (is_mx(mode) ? 1 : 0); }
 
 // Parameters of the split-K decode kernel (weights on the MMA M side,
-// tokens on the N side, 16 tokens per CTA tile).
+// tokens on the N side, 16 or 32 tokens per CTA tile).
 struct DecodeParams {
   const uint8_t* b_img;    // weight image
   const uint8_t* b_sf;     // MX: weight scale image (atoms)
@@ -45,6 +45,7 @@ struct DecodeConfig {
   int mode;
   int sps;     // slabs per stage
   int stages;  // pipeline depth
+  int tok;     // token rows per CTA tile: 16, or 32 (one-slab-per-stage pipelines only)
 };
 
 // Parameters of the large-M kernel (A on the MMA M side, 128 x 256 tiles).

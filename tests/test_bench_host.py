@@ -38,8 +38,8 @@ def test_digest_ignores_comment_edits_and_sees_code_edits(tmp_path):
     # a comment reworded and re-indented: same code, same digest
     assert _digest_of(tmp_path / "b", ("fg_decode.cu", "// Split-K decode GEMM", "//   Split-K  decode  GEMM")) == base
     # one constant changed: a different kernel, a different digest
-    assert _digest_of(tmp_path / "c", ("fg_decode.cu", "constexpr int kTokRows = 16;",
-                                       "constexpr int kTokRows = 32;")) != base
+    assert _digest_of(tmp_path / "c", ("fg_decode.cu", "constexpr int kSlabBytes = 16384;",
+                                       "constexpr int kSlabBytes = 32768;")) != base
     # a change inside a string literal (inline PTX) also counts
     assert _digest_of(tmp_path / "d", ("fg_ptx.cuh", "tcgen05.commit.cta_group::1",
                                        "tcgen05.commit.cta_group::2")) != base

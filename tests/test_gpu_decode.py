@@ -24,7 +24,7 @@ def _slabs(mode, K):
 
 @pytest.mark.parametrize("mode", MODES)
 @pytest.mark.parametrize("M,N,K", [(1, 128, 1536), (3, 384, 1536), (16, 256, 3072), (17, 128, 1536),
-                                   (40, 256, 1024)])
+                                   (24, 384, 1536), (32, 256, 2048), (40, 256, 1024)])
 @pytest.mark.parametrize("S", [1, 2, 4, 8])
 def test_decode_small_shapes(mode, M, N, K, S):
     if S > _slabs(mode, K):
@@ -325,3 +325,73 @@ def test_bounded_wait_reports_timeout_and_context_survives():
             fg.set_wait_timeout_ns(4_000_000_000)
         assert fg.get_error() == fg.FG_OK
         parity.assert_y_close(y_to_f64(c.gemm(split_k=2)), c.ref(), f"{mode} after timeout")
+
+
+# -------------------------------------------------------- 32-token tiles
+
+@pytest.mark.parametrize("M", [17, 32])
+def test_up_to_32_tokens_take_one_token_tile(M):
+    """17..32 tokens run as one 32-token tile (the MMA's N = 32), so the
+    weights stream once; 33..64 take two."""
+    p = fg.gemm_plan("fp8_tensor", M, 16384, 7168)
+    assert p["path"] == 0 and p["tile_m"] == 32
+    assert p["ctas"] == 128 * p["split_k"]
+    p = fg.gemm_plan("fp8_block128", 2 * M, 2048, 7168)      # no large-M form: decode, two 32-token tiles
+    assert p["tile_m"] == 32 and p["ctas"] == 16 * p["split_k"] * 2
+
+
+@pytest.mark.parametrize("mode", MODES)
+@pytest.mark.parametrize("cfg", ["1,4", "1,5", "1,6", "1,8"])
+def test_32_token_pipelines(mode, cfg, monkeypatch):
+    """Every pipeline instantiated for 32-token tiles (one slab per stage),
+    ragged (29 tokens), splits 1 and 3, every output against the oracle."""
+    monkeypatch.setenv("FG_DECODE_CONFIG", cfg)
+    M, N, K = 29, 256, 3072
+    c = Case(mode, *inputs.operands(mode, M, N, K, 710, 711, 712))
+    ref = c.ref()
+    for S in (1, 3):
+        plan = fg.gemm_plan(mode, M, N, K, split_k=S)
+        assert plan["tile_m"] == 32 and f"{plan['stage_slabs']},{plan['stages']}" == cfg
+        parity.assert_y_close(y_to_f64(c.gemm(split_k=S)), ref, f"{mode} {cfg} 32 tokens S={S}")
+    assert fg.get_error() == fg.FG_OK
+
+
+def test_32_token_tiles_refuse_multi_slab_stages(monkeypatch):
+    monkeypatch.setenv("FG_DECODE_CONFIG", "2,3")
+    with pytest.raises(fg.FgError) as e:
+        fg.gemm_plan("fp8_tensor", 20, 2048, 7168)
+    assert e.value.status == fg.FG_ERR_INVALID_ARG
+
+
+@pytest.mark.parametrize("mode", MODES)
+def test_identity_is_bit_exact_32_tokens(mode):
+    M, N, K = 32, 256, 2048
+    _, B, _, b_s = inputs.operands(mode, 1, N, K, 44, 45, 46)
+    if mode == "fp8_block128":
+        b_s = np.full_like(b_s, 0.5)
+    if mode == "fp8_tensor":
+        b_s = np.array([1.0], np.float32)
+    A = np.zeros((M, K), np.uint16 if mode == "bf16" else np.uint8)
+    for m in range(M):
+        A[m, 29 * m + 3] = ONE[mode]
+    if mode == "mxfp4":
+        A = inputs.pack_e2m1(A)
+    c = Case(mode, A, B, _unit_a_scales(mode, M, K), b_s)
+    ref = c.ref()
+    for S in (1, 4):
+        assert np.array_equal(y_to_f64(c.gemm(split_k=S)), parity.bf16_bits_to_f64(oracle.round_bf16(ref)))
+
+
+def test_32_token_bounded_wait_reports_timeout():
+    M, N, K = 20, 256, 2048
+    assert fg.get_error() == fg.FG_OK
+    for mode in ("fp8_tensor", "fp8_block128", "mxfp4"):
+        c = Case(mode, *inputs.operands(mode, M, N, K, 74, 75, 76))
+        fg.set_wait_timeout_ns(20_000_000)
+        try:
+            c.gemm(split_k=2, flags=fg.FG_FLAG_DEBUG_STALL)
+            assert fg.get_error() == fg.FG_ERR_TIMEOUT
+        finally:
+            fg.set_wait_timeout_ns(4_000_000_000)
+        assert fg.get_error() == fg.FG_OK
+        parity.assert_y_close(y_to_f64(c.gemm(split_k=2)), c.ref(), f"{mode} 32 tokens after timeout")
