@@ -184,6 +184,17 @@ int large_tile_m(int mode, int64_t M, int64_t N) {
   return wide_tiles >= sm_count() ? 256 : 128;
 }
 
+// Weight tiles per band of the large-M tile walk (the band stays in L2 while
+// the row blocks of A go by).  FG_LARGE_GROUP_N=<tiles> overrides it (sweep
+// hook).
+int large_group_n() {
+  if (const char* ov = getenv("FG_LARGE_GROUP_N")) {
+    const int g = atoi(ov);
+    if (g >= 1 && g <= 4096) return g;
+  }
+  return 16;
+}
+
 // Large-M MX on CTA pairs (256 x 256 tiles, two SMs per tile): built and
 // correct, but measured 2-6 % slower than the one-CTA 128 x 256 form at the
 // pages' M = 4096 shapes (both are bound by the L2 -> SM stream, see the pair
@@ -650,6 +661,7 @@ fg_status fg_gemm(const void* A, const void* a_scales, int64_t M, const fg_bshuf
     p.KB = static_cast<int>(KBb);
     p.tiles_m = static_cast<int>((M + 255) / 256);
     p.tiles_n = static_cast<int>((N + 255) / 256);
+    p.group_n = large_group_n();
     p.debug_stall = (flags & FG_FLAG_DEBUG_STALL) ? 1 : 0;
     e = launch_relayout_sf_rows(mode, static_cast<const uint8_t*>(a_scales), static_cast<uint8_t*>(workspace), M, K,
                                 st);
@@ -676,6 +688,7 @@ fg_status fg_gemm(const void* A, const void* a_scales, int64_t M, const fg_bshuf
     p.KB = static_cast<int>(rb / 128);
     p.tiles_m = static_cast<int>((M + plan.tile_m - 1) / plan.tile_m);
     p.tiles_n = static_cast<int>(N / 256 + (N % 256 ? 1 : 0));
+    p.group_n = large_group_n();
     p.debug_stall = (flags & FG_FLAG_DEBUG_STALL) ? 1 : 0;
     p.wide = plan.tile_m == 256 ? 1 : 0;
     if (!mx) {

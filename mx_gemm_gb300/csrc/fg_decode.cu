@@ -41,7 +41,7 @@
 // of the tile.  Each CTA's receive area is the stage buffer its last
 // iterations leave idle first; once the MMAs that read that buffer are done,
 // the producer thread tells every peer so (one remote mbarrier arrival each).
-// When a CTA's fp32 partial [128 rows][16 tokens] is in registers and all
+// When a CTA's fp32 partial [128 rows][TOK tokens] is in registers and all
 // peers are ready, its epilogue threads store each row's tokens straight into
 // the owner's receive area (st.async, 16 bytes at a time, counted on the
 // owner's mbarrier).  The owner then sums its rows over the S slices in split

@@ -63,6 +63,7 @@ struct LargeParams {
   int tiles_m, tiles_n;
   int debug_stall;
   int wide;                // bf16 / fp8 per-tensor: 256 x 256 tiles (tiles_m counts 256-row blocks)
+  int group_n;             // weight tiles per band of the tile walk
   // Stream-K tail (bf16 / fp8 per-tensor; sk_iters == 0: all tiles whole).
   // Each CTA first takes dp_rounds whole tiles (c, c + G, ...), then an equal
   // contiguous range of the remaining K iterations.  A tile split between

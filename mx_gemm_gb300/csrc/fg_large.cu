@@ -127,7 +127,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int nch = chunk_count(p, blockIdx.x, gridDim.x, tiles, KB);
       for (int ci = 0; ok && ci < nch; ++ci) {
         const Chunk ch = chunk_at(p, blockIdx.x, gridDim.x, KB, ci);
-        const TileCoord tc = tile_coord(ch.t, p.tiles_m, p.tiles_n);
+        const TileCoord tc = tile_coord(ch.t, p.tiles_m, p.tiles_n, p.group_n);
         const int nslabs_n = min(2, p.N / 128 - 2 * tc.n);  // weight slabs in this tile (1 or 2)
         for (int kb = ch.k0; kb < ch.k1; ++kb, ++it) {
           const int slot = it % kStages;
@@ -212,7 +212,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         break;
       }
       tc_fence_after();
-      const TileCoord tc = tile_coord(ch.t, p.tiles_m, p.tiles_n);
+      const TileCoord tc = tile_coord(ch.t, p.tiles_m, p.tiles_n, p.group_n);
       const int lrow = qd * 32 + lane;
       const int row = tc.m * kBM + lrow;
       const int ncols = min(kBN, p.N - tc.n * kBN);
@@ -386,7 +386,7 @@ __global__ void __launch_bounds__(kWideThreads, 1)
       const int nch = chunk_count(p, blockIdx.x, gridDim.x, tiles, KB);
       for (int ci = 0; ok && ci < nch; ++ci) {
         const Chunk ch = chunk_at(p, blockIdx.x, gridDim.x, KB, ci);
-        const TileCoord tc = tile_coord(ch.t, p.tiles_m, p.tiles_n);
+        const TileCoord tc = tile_coord(ch.t, p.tiles_m, p.tiles_n, p.group_n);
         const int nslabs_n = min(2, p.N / 128 - 2 * tc.n);
         for (int kb = ch.k0; kb < ch.k1; ++kb, ++it) {
           const int slot = it % kWideStages;
@@ -481,7 +481,7 @@ __global__ void __launch_bounds__(kWideThreads, 1)
         break;
       }
       tc_fence_after();
-      const TileCoord tc = tile_coord(ch.t, p.tiles_m, p.tiles_n);
+      const TileCoord tc = tile_coord(ch.t, p.tiles_m, p.tiles_n, p.group_n);
       const int col0 = tc.n * kBN + chalf * 128;
       const int lrow = qd * 32 + lane;
       // stream-K partials: [CTA][half][256 columns][128 rows] fp32
@@ -667,7 +667,7 @@ __global__ void __launch_bounds__(kMxThreads, 1)
       int it = 0;
       bool ok = true;
       for (int t = blockIdx.x; ok && t < tiles; t += gridDim.x) {
-        const TileCoord tc = tile_coord(t, p.tiles_m, p.tiles_n);
+        const TileCoord tc = tile_coord(t, p.tiles_m, p.tiles_n, p.group_n);
         const int nslabs_n = min(2, p.N / 128 - 2 * tc.n);
         for (int kb = 0; kb < KB; ++kb, ++it) {
           const int slot = it % kStages;
@@ -794,7 +794,7 @@ __global__ void __launch_bounds__(kMxThreads, 1)
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&acce_bar);  // accumulator free: the next tile may start
-      const TileCoord tc = tile_coord(t, p.tiles_m, p.tiles_n);
+      const TileCoord tc = tile_coord(t, p.tiles_m, p.tiles_n, p.group_n);
       const int row = tc.m * kBM + qd * 32 + lane;
       const int col0 = tc.n * kBN + half * 128;
       if (row < p.M && col0 < p.N) {

@@ -163,7 +163,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       int it = 0;
       bool ok = true;
       for (int t = pair; ok && t < tiles; t += npairs) {
-        const TileCoord tc = tile_coord(t, p.tiles_m, p.tiles_n);
+        const TileCoord tc = tile_coord(t, p.tiles_m, p.tiles_n, p.group_n);
         const int a128 = 2 * tc.m + static_cast<int>(rank);  // this CTA's 128-row block of A
         const int n128 = 2 * tc.n + static_cast<int>(rank);  // its half of the weight tile
         for (int kb = 0; kb < KB; ++kb, ++it) {
@@ -286,7 +286,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive_remote(&acce_bar, 0);  // the pair's next tile may overwrite the accumulator
-      const TileCoord tc = tile_coord(t, p.tiles_m, p.tiles_n);
+      const TileCoord tc = tile_coord(t, p.tiles_m, p.tiles_n, p.group_n);
       const int row = tc.m * kTileM + static_cast<int>(rank) * 128 + qd * 32 + lane;
       const int col0 = tc.n * kTileN + half * 128;
       if (row < p.M && col0 < p.N) {

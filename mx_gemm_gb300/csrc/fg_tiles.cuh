@@ -6,23 +6,21 @@
 
 namespace fg {
 
-// Tiles are walked in groups of kGroupN weight tiles; inside a group the A row
-// block index runs fastest, so the CTAs resident at one time share a band of
-// weights (kept in L2) and a few A row blocks.
-constexpr int kGroupN = 16;
-
+// Tiles are walked in groups of `group_n` weight tiles; inside a group the
+// weight tile index runs fastest, so the CTAs resident at one time share a
+// band of weights (kept in L2) and a few row blocks of A.
 struct TileCoord {
   int m, n;
 };
 
-__device__ __forceinline__ TileCoord tile_coord(int t, int tiles_m, int tiles_n) {
-  const int per_group = kGroupN * tiles_m;
+__device__ __forceinline__ TileCoord tile_coord(int t, int tiles_m, int tiles_n, int group_n) {
+  const int per_group = group_n * tiles_m;
   const int g = t / per_group;
   const int r = t - g * per_group;
-  const int gn = min(kGroupN, tiles_n - g * kGroupN);
+  const int gn = min(group_n, tiles_n - g * group_n);
   TileCoord c;
   c.m = r / gn;
-  c.n = g * kGroupN + (r - c.m * gn);
+  c.n = g * group_n + (r - c.m * gn);
   return c;
 }
 
