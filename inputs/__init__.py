@@ -201,6 +201,9 @@ WORKLOADS = {
         idx=6, cases=[dict(mode="bf16", M=m, N=n, K=7168, split_k=0) for m, n in DECODE_SHAPES]),
     "mx_fp8a_fp4w_n16384_k7168": dict(
         idx=7, cases=[dict(mode="mxfp4_fp8a", M=m, N=16384, K=7168, split_k=0) for m in (1, 16, 4096)]),
+    # FP8 blockscale at large M
+    "large_fp8_block128_4096x16384x7168": dict(
+        idx=9, cases=[dict(mode="fp8_block128", M=4096, N=16384, K=7168, split_k=1)]),
     # 32 tokens: one 32-token tile per weight tile
     "fp8_tensor_decode_m32_k7168": dict(
         idx=8, cases=[dict(mode="fp8_tensor", M=32, N=n, K=7168, split_k=0) for n in (2048, 16384)]),

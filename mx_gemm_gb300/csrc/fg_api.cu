@@ -299,7 +299,7 @@ uint64_t large_streamk_plan(int mode, int64_t tiles, int64_t KB, int ctas, Large
     p->dp_tiles = 0;
     p->sk_iters = 0;
   }
-  if (is_mx(mode) || ctas <= 0 || tiles <= ctas || tiles % ctas == 0) return 0;
+  if ((mode != FG_BF16 && mode != FG_FP8_TENSOR) || ctas <= 0 || tiles <= ctas || tiles % ctas == 0) return 0;
   const int64_t full_waves = tiles / ctas;
   // 256 x 256 tiles: measured slower (by ~20 us) when every tile is split,
   // i.e. with fewer than two full waves; there the whole-tile schedule is kept
@@ -673,6 +673,8 @@ fg_status fg_gemm(const void* A, const void* a_scales, int64_t M, const fg_bshuf
   }
   if (plan.path == 1) {
     if ((s = make_tmap(&tmap, A, M, rb, 128)) != FG_OK) return s;
+    // the blockscale kernel writes Y by tensor store: boxes of 32 rows x 64 bf16
+    if (mode == FG_FP8_BLOCK128 && (s = make_tmap(&tmap_b, Y, M, N * 2, 32)) != FG_OK) return s;
     LargeParams p;
     memset(&p, 0, sizeof p);
     p.b_img = static_cast<const uint8_t*>(b->data);

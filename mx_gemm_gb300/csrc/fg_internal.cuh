@@ -103,6 +103,9 @@ uint32_t pair_sf_box_rows(int mode);
 cudaError_t launch_large_pair(int mode, const CUtensorMap& tmap_a, const CUtensorMap& tmap_b,
                               const CUtensorMap& tmap_asf, const CUtensorMap& tmap_bsf, const LargeParams& p,
                               int ctas, cudaStream_t stream);
+// One-CTA large-M kernels.  tmap_b: the MXFP4_FP8A weight image's map; for
+// kBlock, the output's map (Y as rows of 2N bytes, boxes of 32 rows x 128
+// bytes, 128-byte swizzle); unused otherwise.
 cudaError_t launch_large(int mode, const CUtensorMap& tmap_a, const CUtensorMap& tmap_b, const LargeParams& p,
                          int ctas, cudaStream_t stream);
 

@@ -832,6 +832,309 @@ cudaError_t launch_mx(const CUtensorMap& tmap_a, const CUtensorMap& tmap_b, cons
   return cudaGetLastError();
 }
 
+// ------------------------------------------------------ FP8 blockscale form
+//
+// FP8 with fp32 scales per (row of A, 128-K block) and per (128 weight rows,
+// 128-K block) -- the aiter PR "FlyDSL split-K preshuffle decode GEMM for
+// small-M shapes" blockscale mode, at large M.  The scales are fp32, not
+// E8M0, so the block-scaled MMA cannot apply them; instead each 128-byte K
+// slab (exactly one 128-K scale block) is multiplied into one of two TMEM
+// partial buffers (the page's gfx942 software-dequant design: one plain MMA
+// pass per scale block), and eight epilogue warps fold every partial into
+// fp32 register accumulators as acc += a_s[row][kb] * b_s[nb][kb] * partial,
+// storing bf16 at the end of the tile.  Per thread: its TMEM lane (a row of
+// A) x 128 of the tile's 256 columns (one 128-row weight block, one b_s).
+// The 128 fp32 accumulators per thread need more registers than an even
+// split of the file gives, so the first warpgroup (producer, MMA issuer, two
+// idle warps) gives registers up to the two epilogue warpgroups:
+// 128 x 24 + 256 x 240 = 384 x 168, the launch's total.
+constexpr int kBlockThreads = 384;
+constexpr int kBlockRegsLow = 24, kBlockRegsHigh = 240;
+static_assert(128 * kBlockRegsLow + 256 * kBlockRegsHigh <= kBlockThreads * 168, "register split over the launch");
+constexpr int kBlockStageOut = 32 * 128;  // per epilogue warp: 32 rows x 64 bf16 columns
+constexpr int kBlockSmem = kStages * kStageBytes + 8 * kBlockStageOut + 1024;
+static_assert(kBlockSmem <= 232448, "shared memory per CTA");
+
+
+__device__ __forceinline__ uint64_t f32x2_splat(float w) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %1};" : "=l"(r) : "f"(w));
+  return r;
+}
+
+// a0 += v0 * w, a1 += v1 * w: two fused multiply-adds, each rounded once
+__device__ __forceinline__ void fma_f32x2(float& a0, float& a1, uint32_t v0, uint32_t v1, uint64_t w2) {
+  asm("{\n .reg .b64 a, v;\n mov.b64 a, {%0, %1};\n mov.b64 v, {%2, %3};\n"
+      " fma.rn.f32x2 a, v, %4, a;\n mov.b64 {%0, %1}, a;\n}"
+      : "+f"(a0), "+f"(a1)
+      : "r"(v0), "r"(v1), "l"(w2));
+}
+
+
+__global__ void __launch_bounds__(kBlockThreads, 1)
+    large_block_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_y,
+                       const LargeParams p) {
+  extern __shared__ uint8_t dsmem[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(dsmem) + 1023) & ~uintptr_t(1023));
+  __shared__ __align__(8) uint64_t full_bar[kStages];
+  __shared__ __align__(8) uint64_t empty_bar[kStages];
+  __shared__ __align__(8) uint64_t pfull_bar[2], pempty_bar[2];  // the two partial buffers
+  __shared__ __align__(8) uint64_t stall_bar, drain_bar;
+  __shared__ uint32_t tmem_base_sh;
+  __shared__ int abort_sh, issued_sh, consumed_sh, mma_any_sh;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int tiles = p.tiles_m * p.tiles_n;
+  const int KB = p.KB;
+  const uint64_t T = p.timeout_ns;
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < kStages; ++i) {
+      mbar_init(&full_bar[i], 1);
+      mbar_init(&empty_bar[i], 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&pfull_bar[i], 1);
+      mbar_init(&pempty_bar[i], 8);  // the eight epilogue warps
+    }
+    mbar_init(&stall_bar, 1);
+    mbar_init(&drain_bar, 1);
+    abort_sh = 0;
+    issued_sh = 0;
+    consumed_sh = 0;
+    mma_any_sh = 0;
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(&tmem_base_sh, kTmemCols);
+    tmem_relinquish();
+  }
+  if (warp == 0 && lane == 0) prefetch_tmap(&tmap_a);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = tmem_base_sh;
+
+  if (warp < 4) {
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kBlockRegsLow));
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      int it = 0;
+      bool ok = true;
+      for (int t = blockIdx.x; ok && t < tiles; t += gridDim.x) {
+        const TileCoord tc = tile_coord(t, p.tiles_m, p.tiles_n, p.group_n);
+        const int nslabs_n = min(2, p.N / 128 - 2 * tc.n);
+        for (int kb = 0; kb < KB; ++kb, ++it) {
+          const int slot = it % kStages;
+          if (!mbar_wait(&empty_bar[slot], ((it / kStages) & 1) ^ 1u, T, p.err, 51)) {
+            ok = false;
+            break;
+          }
+          uint8_t* st = smem + slot * kStageBytes;
+          mbar_arrive_expect_tx(&full_bar[slot], kABytes + nslabs_n * 16384);
+          tma_load_2d(st, &tmap_a, kb * 128, tc.m * kBM, &full_bar[slot]);
+          for (int h = 0; h < nslabs_n; ++h)
+            bulk_g2s(st + kABytes + h * 16384, p.b_img + (static_cast<size_t>(2 * tc.n + h) * KB + kb) * 16384,
+                     16384, &full_bar[slot]);
+        }
+      }
+      issued_sh = it;
+      if (!ok) abort_sh = 1;
+    }
+  } else if (warp == 1) {
+    // ---------------------------------------------------------- MMA issuer
+    if (lane == 0) {
+      bool ok = true;
+      if (p.debug_stall) ok = mbar_wait(&stall_bar, 0, T, p.err, 52);
+      int it = 0;
+      const uint32_t idesc = idesc_e4m3(kBM, kBN);
+      for (int t = blockIdx.x; ok && t < tiles; t += gridDim.x) {
+        for (int kb = 0; kb < KB; ++kb) {
+          const int slot = it % kStages;
+          const int b = it & 1;  // partial buffer of this slab
+          if (!mbar_wait(&full_bar[slot], (it / kStages) & 1, T, p.err, 53) ||
+              !mbar_wait(&pempty_bar[b], ((it >> 1) & 1) ^ 1u, T, p.err, 54)) {
+            ok = false;
+            break;
+          }
+          ++it;  // this stage's copies have landed
+          tc_fence_after();
+          mma_any_sh = 1;
+          uint8_t* st = smem + slot * kStageBytes;
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            const uint64_t adesc = sdesc_sw128(smem_u32(st + j * 32));
+            const uint64_t bdesc = sdesc_sw128(smem_u32(st + kABytes + j * 32));
+            mma_f8f6f4(tmem + b * kBN, adesc, bdesc, idesc, j > 0 ? 1u : 0u);
+          }
+          tc_commit(&pfull_bar[b]);      // the slab's partial is ready
+          tc_commit(&empty_bar[slot]);   // and its stage may be refilled
+        }
+      }
+      consumed_sh = it;
+      if (!ok) abort_sh = 1;
+      if (mma_any_sh) {
+        tc_commit(&drain_bar);
+        mbar_wait(&drain_bar, 0, T, p.err, 55);
+      }
+    }
+  }
+  } else {
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kBlockRegsHigh));
+    // ------------------------------------ epilogue (two warpgroups, 8 warps)
+    // lane quarter warp % 4 (the TMEM lanes this warp may read), column half
+    // (warp - 4) / 4: one 128-row weight block of the 256-column tile
+    const int qd = warp & 3;
+    const int half = (warp - 4) >> 2;
+    const int KS = p.K / 128;
+    const float* a_s = static_cast<const float*>(p.a_scales);
+    // scales are read four slabs at a time, a group ahead of their use
+    const bool vec4 = KS % 4 == 0 && ((reinterpret_cast<uintptr_t>(a_s) | reinterpret_cast<uintptr_t>(p.b_s)) & 15) == 0;
+    // this warp's 32-row x 64-column bf16 staging box (128-byte swizzle)
+    uint8_t* stg = smem + kStages * kStageBytes + (warp - 4) * kBlockStageOut;
+    // scale rows of tile t for this thread (a row past M or a weight block
+    // past N reads row / block 0; nothing of it is stored)
+    auto scale_rows = [&](int t, const float*& arow, const float*& bcol) {
+      const TileCoord tc = tile_coord(t, p.tiles_m, p.tiles_n, p.group_n);
+      const int row = tc.m * kBM + qd * 32 + lane;
+      const int nb = 2 * tc.n + half;
+      arow = a_s + static_cast<size_t>(row < p.M ? row : 0) * KS;
+      bcol = p.b_s + static_cast<size_t>(nb < p.N / 128 ? nb : 0) * KS;
+    };
+    auto load_group = [&](const float* arow, const float* bcol, int kb0, float4& an, float4& bn) {
+      if (vec4) {
+        an = __ldg(reinterpret_cast<const float4*>(arow + kb0));
+        bn = __ldg(reinterpret_cast<const float4*>(bcol + kb0));
+      } else {
+        an.x = __ldg(arow + kb0);
+        bn.x = __ldg(bcol + kb0);
+        an.y = kb0 + 1 < KS ? __ldg(arow + kb0 + 1) : 0.f;
+        bn.y = kb0 + 1 < KS ? __ldg(bcol + kb0 + 1) : 0.f;
+        an.z = kb0 + 2 < KS ? __ldg(arow + kb0 + 2) : 0.f;
+        bn.z = kb0 + 2 < KS ? __ldg(bcol + kb0 + 2) : 0.f;
+        an.w = kb0 + 3 < KS ? __ldg(arow + kb0 + 3) : 0.f;
+        bn.w = kb0 + 3 < KS ? __ldg(bcol + kb0 + 3) : 0.f;
+      }
+    };
+    const float* arow = a_s;
+    const float* bcol = p.b_s;
+    float4 an = make_float4(0.f, 0.f, 0.f, 0.f), bn = an;
+    if (static_cast<int>(blockIdx.x) < tiles) {
+      scale_rows(blockIdx.x, arow, bcol);
+      load_group(arow, bcol, 0, an, bn);
+    }
+    int it = 0;
+    bool ok = true;
+    for (int t = blockIdx.x; ok && t < tiles; t += gridDim.x) {
+      const TileCoord tc = tile_coord(t, p.tiles_m, p.tiles_n, p.group_n);
+      const bool have_nb = 2 * tc.n + half < p.N / 128;
+      const float* ar = arow;
+      const float* bc = bcol;
+      float acc[128];
+#pragma unroll
+      for (int i = 0; i < 128; ++i) acc[i] = 0.f;
+#pragma unroll 1
+      for (int kb0 = 0; ok && kb0 < KB; kb0 += 4) {
+        const float wg[4] = {an.x * bn.x, an.y * bn.y, an.z * bn.z, an.w * bn.w};
+        // the next group's scales (the next tile's first) load while this group runs
+        if (kb0 + 4 < KB) {
+          load_group(ar, bc, kb0 + 4, an, bn);
+        } else if (t + static_cast<int>(gridDim.x) < tiles) {
+          scale_rows(t + gridDim.x, arow, bcol);
+          load_group(arow, bcol, 0, an, bn);
+        }
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          if (kb0 + j >= KB) break;
+          const int b = it & 1;
+          const bool ready = mbar_wait(&pfull_bar[b], (it >> 1) & 1, T, p.err, 56);
+          if (!__all_sync(0xffffffffu, ready)) {
+            ok = false;
+            break;
+          }
+          ++it;
+          tc_fence_after();
+          const uint32_t taddr = tmem + b * kBN + half * 128 + (static_cast<uint32_t>(qd * 32) << 16);
+          const uint64_t w2 = f32x2_splat(wg[j]);
+          // eight 16-column loads; each chunk is folded while the next loads
+          uint32_t va[16], vb[16];
+          tmem_ld16(taddr, va);
+          tmem_wait_ld();
+#pragma unroll
+          for (int c = 1; c < 8; ++c) {
+            if (c & 1) {
+              tmem_ld16(taddr + 16 * c, vb);
+#pragma unroll
+              for (int i = 0; i < 16; i += 2)
+                fma_f32x2(acc[16 * (c - 1) + i], acc[16 * (c - 1) + i + 1], va[i], va[i + 1], w2);
+            } else {
+              tmem_ld16(taddr + 16 * c, va);
+#pragma unroll
+              for (int i = 0; i < 16; i += 2)
+                fma_f32x2(acc[16 * (c - 1) + i], acc[16 * (c - 1) + i + 1], vb[i], vb[i + 1], w2);
+            }
+            tmem_wait_ld();
+          }
+          // the whole partial is in registers: the buffer may take the slab after next
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&pempty_bar[b]);
+#pragma unroll
+          for (int i = 0; i < 16; i += 2) fma_f32x2(acc[112 + i], acc[113 + i], vb[i], vb[i + 1], w2);
+        }
+      }
+      if (!ok) break;
+      if (have_nb) {
+        // bf16 out through the staging box, 64 columns at a time, by tensor
+        // store (rows past M are not written)
+        const int col0 = tc.n * kBN + half * 128;
+#pragma unroll
+        for (int r = 0; r < 2; ++r) {
+          if (lane == 0) bulk_wait_group_read0();  // the previous store has read the box
+          __syncwarp();
+#pragma unroll
+          for (int j = 0; j < 8; ++j) {
+            uint4 o;
+            o.x = pack_bf16x2(acc[64 * r + 8 * j + 0], acc[64 * r + 8 * j + 1]);
+            o.y = pack_bf16x2(acc[64 * r + 8 * j + 2], acc[64 * r + 8 * j + 3]);
+            o.z = pack_bf16x2(acc[64 * r + 8 * j + 4], acc[64 * r + 8 * j + 5]);
+            o.w = pack_bf16x2(acc[64 * r + 8 * j + 6], acc[64 * r + 8 * j + 7]);
+            *reinterpret_cast<uint4*>(stg + lane * 128 + ((j ^ (lane & 7)) << 4)) = o;
+          }
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) {
+            tma_store_2d(&tmap_y, stg, (col0 + 64 * r) * 2, tc.m * kBM + qd * 32);
+            bulk_commit_group();
+          }
+        }
+      }
+    }
+    if (lane == 0) bulk_wait_group0();  // every store has landed
+    if (!ok && lane == 0) abort_sh = 1;
+  }
+
+  // ------------------------------------------------------------- teardown
+  tc_fence_before();
+  __syncthreads();
+  if (abort_sh && threadIdx.x == 0) {
+    for (int it = consumed_sh; it < issued_sh; ++it)
+      mbar_wait(&full_bar[it % kStages], (it / kStages) & 1, T, nullptr, 0);
+  }
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 1) tmem_dealloc(tmem, kTmemCols);
+}
+
+cudaError_t launch_block(const CUtensorMap& tmap_a, const CUtensorMap& tmap_y, const LargeParams& p, int ctas,
+                         cudaStream_t stream) {
+  cudaError_t e = ensure_smem_attr(reinterpret_cast<const void*>(&large_block_kernel), kBlockSmem);
+  if (e != cudaSuccess) return e;
+  large_block_kernel<<<ctas, kBlockThreads, kBlockSmem, stream>>>(tmap_a, tmap_y, p);
+  return cudaGetLastError();
+}
+
 }  // namespace
 
 uint64_t large_streamk_bytes(int ctas, bool wide) {
@@ -839,7 +1142,7 @@ uint64_t large_streamk_bytes(int ctas, bool wide) {
               : static_cast<uint64_t>(ctas) * (static_cast<uint64_t>(kBN) * kBM * 4 + 4 * 8);
 }
 
-bool large_supported(int mode) { return mode == kBF16 || mode == kTensor || is_mx(mode); }
+bool large_supported(int mode) { return mode == kBF16 || mode == kTensor || mode == kBlock || is_mx(mode); }
 
 cudaError_t launch_large(int mode, const CUtensorMap& tmap_a, const CUtensorMap& tmap_b, const LargeParams& p,
                          int ctas, cudaStream_t stream) {
@@ -848,6 +1151,7 @@ cudaError_t launch_large(int mode, const CUtensorMap& tmap_a, const CUtensorMap&
     if (mode == kTensor) return launch_wide<kTensor>(tmap_a, p, ctas, stream);
     return cudaErrorNotSupported;
   }
+  if (mode == kBlock) return launch_block(tmap_a, tmap_b, p, ctas, stream);  // tmap_b: the output's map
   if (mode == kBF16) return launch_mode<kBF16>(tmap_a, p, ctas, stream);
   if (mode == kTensor) return launch_mode<kTensor>(tmap_a, p, ctas, stream);
   if (mode == kMXFP8) return launch_mx<kMXFP8>(tmap_a, tmap_b, p, ctas, stream);

@@ -336,8 +336,8 @@ def test_up_to_32_tokens_take_one_token_tile(M):
     p = fg.gemm_plan("fp8_tensor", M, 16384, 7168)
     assert p["path"] == 0 and p["tile_m"] == 32
     assert p["ctas"] == 128 * p["split_k"]
-    p = fg.gemm_plan("fp8_block128", 2 * M, 2048, 7168)      # no large-M form: decode, two 32-token tiles
-    assert p["tile_m"] == 32 and p["ctas"] == 16 * p["split_k"] * 2
+    p = fg.gemm_plan("fp8_tensor", 2 * M, 2048, 7168, split_k=2)  # an explicit split keeps decode: two tiles
+    assert p["path"] == 0 and p["tile_m"] == 32 and p["ctas"] == 16 * 2 * 2
 
 
 @pytest.mark.parametrize("mode", MODES)

@@ -19,7 +19,7 @@ from tests.gpu_util import Case, y_to_f64
 pytestmark = pytest.mark.gpu
 
 
-@pytest.mark.parametrize("mode", ["bf16", "fp8_tensor", "mxfp8", "mxfp4", "mxfp8_b32", "mxfp4_fp8a"])
+@pytest.mark.parametrize("mode", ["bf16", "fp8_tensor", "fp8_block128", "mxfp8", "mxfp4", "mxfp8_b32", "mxfp4_fp8a"])
 @pytest.mark.parametrize("M,N,K", [(33, 256, 512), (129, 384, 1024), (300, 512, 2048), (1000, 1280, 1536)])
 def test_large_small_shapes(mode, M, N, K):
     c = Case(mode, *inputs.operands(mode, M, N, K, 10 + M, 20 + N, 30 + K))
@@ -28,7 +28,8 @@ def test_large_small_shapes(mode, M, N, K):
     parity.assert_y_close(y_to_f64(c.gemm()), c.ref(), f"{mode} {M}x{N}x{K}")
 
 
-@pytest.mark.parametrize("mode", ["bf16", "fp8_tensor", "mxfp8", "mxfp4", "mxfp8_b32", "mxfp4_fp8a"])
+@pytest.mark.parametrize("mode", ["bf16", "fp8_tensor", "fp8_block128", "mxfp8", "mxfp4", "mxfp8_b32",
+                                  "mxfp4_fp8a"])
 def test_large_identity_is_bit_exact(mode):
     M, N, K = 300, 512, 1024
     _, B, _, b_s = inputs.operands(mode, 1, N, K, 3, 4, 5)
@@ -39,6 +40,8 @@ def test_large_identity_is_bit_exact(mode):
     a_s = None
     if mode == "fp8_tensor":
         a_s, b_s = np.array([1.0], np.float32), np.array([1.0], np.float32)
+    elif mode == "fp8_block128":
+        a_s, b_s = np.ones((M, K // 128), np.float32), np.full_like(b_s, 0.5)
     elif mode == "mxfp8":
         a_s = np.full((M, K // 128), 127, np.uint8)
     elif mode == "mxfp4":
@@ -58,6 +61,7 @@ def test_large_identity_is_bit_exact(mode):
     ("mxfp4", 4096, 16384, 7168, "mx_mxfp8_mxfp4_n16384_k7168", 5),
     ("mxfp4_fp8a", 4096, 16384, 7168, "mx_fp8a_fp4w_n16384_k7168", 2),
     ("mxfp8_b32", 4096, 16384, 7168, "mx_mxfp8_b32_n16384_k7168", 2),
+    ("fp8_block128", 4096, 16384, 7168, "large_fp8_block128_4096x16384x7168", 0),
 ])
 def test_large_workload_parity_sampled_rows(mode, M, N, K, name, idx):
     A, B, a_s, b_s = inputs.workload_operands(name, idx)
@@ -101,6 +105,7 @@ def test_streamk_tail_matches_whole_tiles(mode, tile, M, N, K, monkeypatch):
     ("fp8_tensor", 2560, 2048, 1024, True),    # stream-K tail: cooperative CTAs that wait on one another
     ("bf16", 300, 512, 1024, False),
     ("mxfp4", 300, 512, 1024, False),
+    ("fp8_block128", 300, 512, 1024, False),
 ])
 def test_large_bounded_wait_reports_timeout(mode, M, N, K, streamk):
     """The MMA issuer waits on a barrier nothing arrives at: every wait of the
@@ -111,6 +116,7 @@ def test_large_bounded_wait_reports_timeout(mode, M, N, K, streamk):
     assert fg.get_error() == fg.FG_OK
     ws = torch.empty(max(4, fg.gemm_workspace_size(mode, M, N, K)) // 4, dtype=torch.float32, device="cuda")
     assert (fg.gemm_workspace_size(mode, M, N, K) > 0) == (streamk or mode == "mxfp4")
+    assert fg.gemm_plan(mode, M, N, K)["path"] == 1
     fg.set_wait_timeout_ns(20_000_000)
     try:
         c.gemm(workspace=ws, flags=fg.FG_FLAG_DEBUG_STALL)
