@@ -274,8 +274,22 @@ __global__ void __launch_bounds__(kThreads, (DCfg<MODE, SPS, STAGES, TOK>::MIN_C
         }
       }
       if (it + 1 == pre) {
-        // weights of the first stages are on their way: now wait for the
-        // previous kernel, then fetch the token tiles of those stages
+        // Weights of the first stages are on their way.  When the rest of
+        // this CTA's K range is short (at most one more window: the latency-
+        // bound shapes), its weights and the token tiles go to L2 meanwhile.
+        // A prefetch only warms L2, which every writer of the tokens goes
+        // through, so it cannot hand out stale data; the copies into shared
+        // memory still wait for the previous kernel.
+        if (lane == 0 && nslab <= 2 * pre * SPS) {
+          const int ub = pre * SPS;
+          const int wb = C::FP4W ? kFp4SlabBytes : kSlabBytes;
+          if (nslab > ub)
+            prefetch_l2(p.b_img + (static_cast<size_t>(nt) * p.KB + u0 + ub) * wb,
+                        static_cast<uint32_t>((nslab - ub) * wb));
+          for (int u = 0; u < nslab; ++u) prefetch_l2_box(&tmap_a, (u0 + u) * 128, mt * kTokRows);
+        }
+        // now wait for the previous kernel, then fetch the token tiles of the
+        // first stages
         pdl_wait();
         if (lane == 0) {
           for (int jt = 0; jt < pre; ++jt) {
