@@ -28,6 +28,30 @@ def test_large_small_shapes(mode, M, N, K):
     parity.assert_y_close(y_to_f64(c.gemm()), c.ref(), f"{mode} {M}x{N}x{K}")
 
 
+@pytest.mark.parametrize("M,N,K", [(300, 512, 640), (129, 384, 1152), (40, 256, 384)])
+def test_large_blockscale_ragged_scale_blocks(M, N, K):
+    """K/128 not a multiple of 4: the large-M blockscale epilogue reads its
+    scale products one by one instead of four at a time."""
+    mode = "fp8_block128"
+    c = Case(mode, *inputs.operands(mode, M, N, K, 40 + M, 50 + N, 60 + K))
+    assert fg.gemm_plan(mode, M, N, K)["path"] == 1
+    parity.assert_y_close(y_to_f64(c.gemm()), c.ref(), f"{mode} {M}x{N}x{K}")
+
+
+def test_large_blockscale_scales_not_16_byte_aligned():
+    """A scales that are 4-byte but not 16-byte aligned (a view one float into
+    a buffer) take the scalar scale reads; the result is the same."""
+    mode, M, N, K = "fp8_block128", 300, 512, 1024
+    c = Case(mode, *inputs.operands(mode, M, N, K, 70, 71, 72))
+    buf = torch.zeros(M * (K // 128) + 1, dtype=torch.float32, device="cuda")
+    a_s = buf[1:].view(M, K // 128)
+    a_s.copy_(c.da_s)
+    assert a_s.data_ptr() % 16 != 0
+    Y = fg.gemm(c.dA, c.pb, a_s)
+    assert np.array_equal(y_to_f64(Y), y_to_f64(c.gemm()))
+    parity.assert_y_close(y_to_f64(Y), c.ref(), "misaligned A scales")
+
+
 @pytest.mark.parametrize("mode", ["bf16", "fp8_tensor", "fp8_block128", "mxfp8", "mxfp4", "mxfp8_b32",
                                   "mxfp4_fp8a"])
 def test_large_identity_is_bit_exact(mode):
