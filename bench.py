@@ -41,7 +41,7 @@ def _wl(src, first, n, kind):
 
 
 WORKLOADS = {
-    # the pages' first decode configuration as stated: split_k fixed at 4
+    # M=1 N=2048 K=7168 with an explicit split_k of 4
     "fp8_tensor_decode_m1_n2048_k7168_split4": _wl("fp8_tensor_decode_m1_n2048_k7168_split4", 0, 1, "decode"),
     "fp8_tensor_decode_sweep_k7168": _wl("fp8_tensor_decode_sweep_k7168", 0, 4, "decode"),
     "large_bf16_54560x8192x8192": _wl("large_bf16_54560x8192x8192_fp8_4096x4096x8192", 0, 1, "large"),
@@ -56,6 +56,7 @@ WORKLOADS = {
     "bf16_decode_sweep_k7168": _wl("bf16_decode_sweep_k7168", 0, 4, "decode"),
     "fp8_tensor_decode_m32_k7168": _wl("fp8_tensor_decode_m32_k7168", 0, 2, "decode"),
     "large_fp8_block128_4096x16384x7168": _wl("large_fp8_block128_4096x16384x7168", 0, 1, "large"),
+    "large_fp8_block128_4096x8192x7168": _wl("large_fp8_block128_4096x8192x7168", 0, 1, "large"),
     # fp8 activations against fp4 weights, on the MX shapes
     "mxfp4_fp8a_decode_n16384_k7168": _wl("mx_fp8a_fp4w_n16384_k7168", 0, 2, "decode"),
     "large_mxfp4_fp8a_4096x16384x7168": _wl("mx_fp8a_fp4w_n16384_k7168", 2, 1, "large"),
