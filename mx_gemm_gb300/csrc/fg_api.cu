@@ -424,15 +424,15 @@ cudaError_t ensure_smem_attr(const void* kernel, int bytes) {
 }
 
 int sm_count() {
-  static int count[64] = {};
+  static std::atomic<int> count[64];  // per device, looked up once (threads may race to the same value)
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 148;
-  if (!count[dev]) {
-    int c = 0;
+  int c = count[dev].load(std::memory_order_relaxed);
+  if (!c) {
     if (cudaDeviceGetAttribute(&c, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || c <= 0) c = 148;
-    count[dev] = c;
+    count[dev].store(c, std::memory_order_relaxed);
   }
-  return count[dev];
+  return c;
 }
 
 }  // namespace fg

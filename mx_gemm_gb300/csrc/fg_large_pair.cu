@@ -44,6 +44,7 @@
 // that either producer started complete (arming phases only the odd CTA
 // started, standing in for the bytes of copies the odd CTA never issued)
 // before the pair releases its shared and tensor memory.
+#include <atomic>
 #include <cuda_bf16.h>
 
 #include "fg_internal.cuh"
@@ -359,10 +360,10 @@ cudaError_t launch_pair(const CUtensorMap& tmap_a, const CUtensorMap& tmap_b, co
 }  // namespace
 
 int pair_max_clusters() {
-  static int cached[64] = {};
+  static std::atomic<int> cached[64];  // per device, computed once (threads may race to the same value)
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
-  if (cached[dev]) return cached[dev];
+  if (const int c = cached[dev].load(std::memory_order_relaxed)) return c;
   using C = PairCfg<kMXFP4>;  // the largest shared-memory footprint of the pair kernels
   if (ensure_smem_attr(reinterpret_cast<const void*>(&large_mx_pair_kernel<kMXFP4>), C::SMEM) != cudaSuccess)
     return 0;
@@ -382,7 +383,7 @@ int pair_max_clusters() {
           cudaSuccess ||
       n <= 0)
     return 0;
-  cached[dev] = n;
+  cached[dev].store(n, std::memory_order_relaxed);
   return n;
 }
 
