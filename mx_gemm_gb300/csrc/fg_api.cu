@@ -357,6 +357,22 @@ fg_status make_tmap(CUtensorMap* map, const void* base, int64_t rows, int64_t rb
   return FG_OK;
 }
 
+// The bf16 output Y [rows][n] as rows of 2n bytes, boxes of 32 rows x 64
+// bytes (32 columns) in the 64-byte swizzle: the store map of the large-M MX
+// and 128 x 256 bf16 / fp8 kernels.
+fg_status make_tmap_out64(CUtensorMap* map, void* y, int64_t rows, int64_t n) {
+  auto fn = encode_fn();
+  if (!fn) return fail(FG_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
+  cuuint64_t dims[2] = {static_cast<cuuint64_t>(2 * n), static_cast<cuuint64_t>(rows)};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(2 * n)};
+  cuuint32_t box[2] = {64, 32};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, y, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                  CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return fail(FG_ERR_CUDA, "cuTensorMapEncodeTiled (output) failed (%d)", static_cast<int>(r));
+  return FG_OK;
+}
+
 // Plain (unswizzled) 2-D map over `rows` rows of `rbytes` bytes (a multiple
 // of 8, at most 2048) in 8-byte elements, with a box of box_rows whole rows:
 // the weight image as 2 KiB rows (a 16 KiB slab is 8 of them) or a scale
@@ -673,8 +689,12 @@ fg_status fg_gemm(const void* A, const void* a_scales, int64_t M, const fg_bshuf
   }
   if (plan.path == 1) {
     if ((s = make_tmap(&tmap, A, M, rb, 128)) != FG_OK) return s;
-    // the blockscale kernel writes Y by tensor store: boxes of 32 rows x 64 bf16
-    if (mode == FG_FP8_BLOCK128 && (s = make_tmap(&tmap_b, Y, M, N * 2, 32)) != FG_OK) return s;
+    // every large-M kernel writes Y by tensor store: boxes of 32 rows x 64
+    // bf16 (blockscale, 256 x 256) or 32 rows x 32 (MX and 128 x 256 bf16 /
+    // fp8, whose stages leave less room)
+    CUtensorMap tmap_y;
+    const bool box64 = mode == FG_FP8_BLOCK128 || plan.tile_m == 256;
+    if ((s = box64 ? make_tmap(&tmap_y, Y, M, N * 2, 32) : make_tmap_out64(&tmap_y, Y, M, N)) != FG_OK) return s;
     LargeParams p;
     memset(&p, 0, sizeof p);
     p.b_img = static_cast<const uint8_t*>(b->data);
@@ -712,7 +732,7 @@ fg_status fg_gemm(const void* A, const void* a_scales, int64_t M, const fg_bshuf
       if (e != cudaSuccess) return cuda_fail(e, "A scale relayout launch");
       p.a_sf = static_cast<const uint8_t*>(workspace);
     }
-    e = launch_large(mode, tmap, tmap_b, p, plan.ctas, st);
+    e = launch_large(mode, tmap, tmap_b, tmap_y, p, plan.ctas, st);
     if (e != cudaSuccess) return cuda_fail(e, "large-M kernel launch");
     return FG_OK;
   }

@@ -103,11 +103,14 @@ uint32_t pair_sf_box_rows(int mode);
 cudaError_t launch_large_pair(int mode, const CUtensorMap& tmap_a, const CUtensorMap& tmap_b,
                               const CUtensorMap& tmap_asf, const CUtensorMap& tmap_bsf, const LargeParams& p,
                               int ctas, cudaStream_t stream);
-// One-CTA large-M kernels.  tmap_b: the MXFP4_FP8A weight image's map; for
-// kBlock, the output's map (Y as rows of 2N bytes, boxes of 32 rows x 128
-// bytes, 128-byte swizzle); unused otherwise.
-cudaError_t launch_large(int mode, const CUtensorMap& tmap_a, const CUtensorMap& tmap_b, const LargeParams& p,
-                         int ctas, cudaStream_t stream);
+// One-CTA large-M kernels.  tmap_b: the MXFP4_FP8A weight image's map
+// (unused otherwise).  tmap_y: the output Y as rows of 2N bytes; all these
+// kernels write their bf16 tiles by tensor store -- kBlock and the 256 x 256
+// form (p.wide): boxes of 32 rows x 128 bytes, 128-byte swizzle; the MX
+// modes and the 128 x 256 bf16 / fp8 form: boxes of 32 rows x 64 bytes,
+// 64-byte swizzle.
+cudaError_t launch_large(int mode, const CUtensorMap& tmap_a, const CUtensorMap& tmap_b, const CUtensorMap& tmap_y,
+                         const LargeParams& p, int ctas, cudaStream_t stream);
 
 cudaError_t launch_relayout_b(const uint8_t* src, uint8_t* dst, int64_t N, int64_t Kb, bool inverse,
                               cudaStream_t stream);

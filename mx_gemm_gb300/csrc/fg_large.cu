@@ -43,6 +43,8 @@ constexpr int kABytes = kBM * 128;        // 16 KiB
 constexpr int kBBytes = kBN * 128;        // 32 KiB
 constexpr int kStageBytes = kABytes + kBBytes;
 constexpr int kSmem = kStages * kStageBytes + 1024;
+// the 128 x 256 bf16 / fp8 form: + a 32-row x 32-column bf16 staging box per epilogue warp
+constexpr int kSmemOut = kSmem + 4 * 32 * 64;
 constexpr int kTmemCols = 512;            // two 256-column accumulators
 static_assert(kSmem <= 232448, "shared memory budget");
 
@@ -75,8 +77,11 @@ __device__ __forceinline__ Chunk chunk_at(const LargeParams& p, int c, int G, in
 }
 
 template <int MODE>
+// tmap_y: Y as rows of 2N bytes, boxes of 32 rows x 64 bytes (64-byte
+// swizzle): the bf16 tiles leave by tensor store.
 __global__ void __launch_bounds__(kThreads, 1)
-    large_kernel(const __grid_constant__ CUtensorMap tmap_a, const LargeParams p) {
+    large_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_y,
+                 const LargeParams p) {
   extern __shared__ uint8_t dsmem[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(dsmem) + 1023) & ~uintptr_t(1023));
   __shared__ __align__(8) uint64_t full_bar[kStages];
@@ -202,6 +207,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int qd = warp & 3;
     float scale = 1.f;
     if (MODE == kTensor) scale = __ldg(static_cast<const float*>(p.a_scales)) * __ldg(p.b_s);
+    // this warp's 32-row x 32-column bf16 staging box (64-byte swizzle)
+    uint8_t* stg = smem + kStages * kStageBytes + (warp - 2) * (32 * 64);
     const int nch = chunk_count(p, blockIdx.x, gridDim.x, tiles, KB);
     for (int ti = 0; ti < nch; ++ti) {
       const Chunk ch = chunk_at(p, blockIdx.x, gridDim.x, KB, ti);
@@ -243,7 +250,6 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (have_peer) (void)ld_acquire_u64(p.sk_flag + (blockIdx.x + 1) * 4 + qd);
           else if (lane == 0) abort_sh = 1;
         }
-        __nv_bfloat16* yrow = p.y + static_cast<size_t>(row) * p.N + static_cast<size_t>(tc.n) * kBN;
         for (int c = 0; c < ncols; c += 32) {
           uint32_t v[32];
           tmem_ld32(taddr + c, v);
@@ -255,8 +261,11 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int i = 0; i < 32; ++i) f[i] += __ldcg(peer + (c + i) * kBM + lrow);
           }
-          if (row < p.M && have_peer) {
-            uint4* dst = reinterpret_cast<uint4*>(yrow + c);
+          if (have_peer) {
+            // bf16 out through the staging box by tensor store (rows past M
+            // are not written)
+            if (lane == 0) bulk_wait_group_read0();  // the previous store has read the box
+            __syncwarp();
 #pragma unroll
             for (int q = 0; q < 4; ++q) {
               uint4 o;
@@ -264,7 +273,14 @@ __global__ void __launch_bounds__(kThreads, 1)
               o.y = pack_bf16x2(f[8 * q + 2] * scale, f[8 * q + 3] * scale);
               o.z = pack_bf16x2(f[8 * q + 4] * scale, f[8 * q + 5] * scale);
               o.w = pack_bf16x2(f[8 * q + 6] * scale, f[8 * q + 7] * scale);
-              dst[q] = o;
+              // 64-byte rows, 16-byte chunk q at q ^ (row / 2 % 4)
+              *reinterpret_cast<uint4*>(stg + lane * 64 + ((q ^ ((lane >> 1) & 3)) << 4)) = o;
+            }
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+              tma_store_2d(&tmap_y, stg, (tc.n * kBN + c) * 2, tc.m * kBM + qd * 32);
+              bulk_commit_group();
             }
           }
         }
@@ -279,6 +295,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(&acce_bar[acc]);
     }
+    if (lane == 0) bulk_wait_group0();  // every store has landed
   }
 
   // ------------------------------------------------------------- teardown
@@ -294,20 +311,21 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 template <int MODE>
-cudaError_t launch_mode(const CUtensorMap& tmap_a, const LargeParams& p, int ctas, cudaStream_t stream) {
-  cudaError_t e = ensure_smem_attr(reinterpret_cast<const void*>(&large_kernel<MODE>), kSmem);
+cudaError_t launch_mode(const CUtensorMap& tmap_a, const CUtensorMap& tmap_y, const LargeParams& p, int ctas,
+                        cudaStream_t stream) {
+  cudaError_t e = ensure_smem_attr(reinterpret_cast<const void*>(&large_kernel<MODE>), kSmemOut);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(ctas);
   cfg.blockDim = dim3(kThreads);
-  cfg.dynamicSmemBytes = kSmem;
+  cfg.dynamicSmemBytes = kSmemOut;
   cfg.stream = stream;
   cudaLaunchAttribute attr;
   attr.id = cudaLaunchAttributeCooperative;  // stream-K CTAs wait on one another: all must be resident
   attr.val.cooperative = 1;
   cfg.attrs = &attr;
   cfg.numAttrs = p.sk_iters > 0 ? 1 : 0;
-  return cudaLaunchKernelEx(&cfg, large_kernel<MODE>, tmap_a, p);
+  return cudaLaunchKernelEx(&cfg, large_kernel<MODE>, tmap_a, tmap_y, p);
 }
 
 
@@ -332,12 +350,16 @@ constexpr int kWideBM = 256;
 constexpr int kWideStages = 3;
 constexpr int kWideABytes = kWideBM * 128;  // 32 KiB
 constexpr int kWideStageBytes = kWideABytes + kBBytes;
-constexpr int kWideSmem = kWideStages * kWideStageBytes + 1024;
+constexpr int kWideStageOut = 32 * 128;  // per epilogue warp: a 32-row x 64-column bf16 staging box
+constexpr int kWideSmem = kWideStages * kWideStageBytes + 8 * kWideStageOut + 1024;
 static_assert(kWideSmem <= 232448, "shared memory budget");
 
+// tmap_y: Y as rows of 2N bytes, boxes of 32 rows x 128 bytes (128-byte
+// swizzle): the bf16 tiles leave by tensor store.
 template <int MODE>
 __global__ void __launch_bounds__(kWideThreads, 1)
-    large_wide_kernel(const __grid_constant__ CUtensorMap tmap_a, const LargeParams p) {
+    large_wide_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_y,
+                      const LargeParams p) {
   extern __shared__ uint8_t dsmem[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(dsmem) + 1023) & ~uintptr_t(1023));
   __shared__ __align__(8) uint64_t full_bar[kWideStages];
@@ -472,6 +494,7 @@ __global__ void __launch_bounds__(kWideThreads, 1)
     float scale = 1.f;
     if (MODE == kTensor) scale = __ldg(static_cast<const float*>(p.a_scales)) * __ldg(p.b_s);
     const int ew = warp - 2;  // epilogue warp 0..7: its stream-K flag
+    uint8_t* stg = smem + kWideStages * kWideStageBytes + ew * kWideStageOut;
     const int nch = chunk_count(p, blockIdx.x, gridDim.x, tiles, KB);
     for (int ti = 0; ti < nch; ++ti) {
       const Chunk ch = chunk_at(p, blockIdx.x, gridDim.x, KB, ti);
@@ -519,17 +542,30 @@ __global__ void __launch_bounds__(kWideThreads, 1)
 #pragma unroll
           for (int i = 0; i < 128; ++i) v[i] = __float_as_uint(__uint_as_float(v[i]) + __ldcg(peer + i * kBM));
         }
-        const int row = tc.m * kWideBM + h * kBM + lrow;
-        if (row < p.M && col0 < p.N && have_peer) {
-          uint4* dst = reinterpret_cast<uint4*>(p.y + static_cast<size_t>(row) * p.N + col0);
+        if (col0 < p.N && have_peer) {
+          // bf16 out through this warp's staging box, 64 columns at a time,
+          // by tensor store (rows past M are not written)
+          const int row0 = tc.m * kWideBM + h * kBM + qd * 32;
 #pragma unroll
-          for (int q = 0; q < 16; ++q) {
-            uint4 o;
-            o.x = pack_bf16x2(__uint_as_float(v[8 * q + 0]) * scale, __uint_as_float(v[8 * q + 1]) * scale);
-            o.y = pack_bf16x2(__uint_as_float(v[8 * q + 2]) * scale, __uint_as_float(v[8 * q + 3]) * scale);
-            o.z = pack_bf16x2(__uint_as_float(v[8 * q + 4]) * scale, __uint_as_float(v[8 * q + 5]) * scale);
-            o.w = pack_bf16x2(__uint_as_float(v[8 * q + 6]) * scale, __uint_as_float(v[8 * q + 7]) * scale);
-            dst[q] = o;
+          for (int r = 0; r < 2; ++r) {
+            if (lane == 0) bulk_wait_group_read0();  // the previous store has read the box
+            __syncwarp();
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+              const int q = 8 * r + j;
+              uint4 o;
+              o.x = pack_bf16x2(__uint_as_float(v[8 * q + 0]) * scale, __uint_as_float(v[8 * q + 1]) * scale);
+              o.y = pack_bf16x2(__uint_as_float(v[8 * q + 2]) * scale, __uint_as_float(v[8 * q + 3]) * scale);
+              o.z = pack_bf16x2(__uint_as_float(v[8 * q + 4]) * scale, __uint_as_float(v[8 * q + 5]) * scale);
+              o.w = pack_bf16x2(__uint_as_float(v[8 * q + 6]) * scale, __uint_as_float(v[8 * q + 7]) * scale);
+              *reinterpret_cast<uint4*>(stg + lane * 128 + ((j ^ (lane & 7)) << 4)) = o;
+            }
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+              tma_store_2d(&tmap_y, stg, (col0 + 64 * r) * 2, row0);
+              bulk_commit_group();
+            }
           }
         }
       }
@@ -544,6 +580,7 @@ __global__ void __launch_bounds__(kWideThreads, 1)
         if (lane == 0) p.sk_flag[(blockIdx.x + 1) * 8 + ew] = 0;
       }
     }
+    if (lane == 0) bulk_wait_group0();  // every store has landed
   }
 
   // ------------------------------------------------------------- teardown
@@ -559,7 +596,8 @@ __global__ void __launch_bounds__(kWideThreads, 1)
 }
 
 template <int MODE>
-cudaError_t launch_wide(const CUtensorMap& tmap_a, const LargeParams& p, int ctas, cudaStream_t stream) {
+cudaError_t launch_wide(const CUtensorMap& tmap_a, const CUtensorMap& tmap_y, const LargeParams& p, int ctas,
+                        cudaStream_t stream) {
   cudaError_t e = ensure_smem_attr(reinterpret_cast<const void*>(&large_wide_kernel<MODE>), kWideSmem);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
@@ -572,7 +610,7 @@ cudaError_t launch_wide(const CUtensorMap& tmap_a, const LargeParams& p, int cta
   attr.val.cooperative = 1;
   cfg.attrs = &attr;
   cfg.numAttrs = p.sk_iters > 0 ? 1 : 0;
-  return cudaLaunchKernelEx(&cfg, large_wide_kernel<MODE>, tmap_a, p);
+  return cudaLaunchKernelEx(&cfg, large_wide_kernel<MODE>, tmap_a, tmap_y, p);
 }
 
 
@@ -600,7 +638,8 @@ struct MxCfg {
   static constexpr int SFB_BYTES = 2 * APS * 512;
   static constexpr int STAGE_RAW = kABytes + kBBytes + SFA_BYTES + SFB_BYTES;
   static constexpr int STAGE_BYTES = (STAGE_RAW + 1023) / 1024 * 1024;
-  static constexpr int SMEM = kStages * STAGE_BYTES + 1024;
+  static constexpr int OUT_BYTES = 8 * 32 * 64;  // per epilogue warp: a 32-row x 32-column bf16 staging box
+  static constexpr int SMEM = kStages * STAGE_BYTES + OUT_BYTES + 1024;
   static constexpr int SF_COLS = APS * 4 + APS * 8;  // TMEM columns per stage: A (128 rows) + B (256 rows)
   // mxfp8: one atom holds four slabs' scales, so the scales are copied at
   // the first slab of each group of four, into a ring of four group buffers
@@ -616,7 +655,7 @@ struct MxCfg {
 template <int MODE>
 __global__ void __launch_bounds__(kMxThreads, 1)
     large_mx_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_b,
-                    const LargeParams p) {
+                    const __grid_constant__ CUtensorMap tmap_y, const LargeParams p) {
   using C = MxCfg<MODE>;
   extern __shared__ uint8_t dsmem[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(dsmem) + 1023) & ~uintptr_t(1023));
@@ -776,6 +815,8 @@ __global__ void __launch_bounds__(kMxThreads, 1)
     // eight epilogue warps: lane quarter warp % 4, column half (warp - 2) / 4
     const int qd = warp & 3;
     const int half = (warp - 2) >> 2;
+    // this warp's 32-row x 32-column bf16 staging box (64-byte swizzle)
+    uint8_t* stg = smem + kStages * C::STAGE_BYTES + (warp - 2) * (32 * 64);
     int ti = 0;
     for (int t = blockIdx.x; t < tiles; t += gridDim.x, ++ti) {
       const bool w = mbar_wait(&accf_bar, ti & 1, T, p.err, 26);
@@ -795,21 +836,35 @@ __global__ void __launch_bounds__(kMxThreads, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(&acce_bar);  // accumulator free: the next tile may start
       const TileCoord tc = tile_coord(t, p.tiles_m, p.tiles_n, p.group_n);
-      const int row = tc.m * kBM + qd * 32 + lane;
       const int col0 = tc.n * kBN + half * 128;
-      if (row < p.M && col0 < p.N) {
-        uint4* dst = reinterpret_cast<uint4*>(p.y + static_cast<size_t>(row) * p.N + col0);
+      if (col0 < p.N) {
+        // bf16 out through the staging box, 32 columns at a time, by tensor
+        // store (rows past M are not written)
 #pragma unroll
-        for (int q = 0; q < 16; ++q) {
-          uint4 o;
-          o.x = pack_bf16x2(__uint_as_float(v[8 * q + 0]), __uint_as_float(v[8 * q + 1]));
-          o.y = pack_bf16x2(__uint_as_float(v[8 * q + 2]), __uint_as_float(v[8 * q + 3]));
-          o.z = pack_bf16x2(__uint_as_float(v[8 * q + 4]), __uint_as_float(v[8 * q + 5]));
-          o.w = pack_bf16x2(__uint_as_float(v[8 * q + 6]), __uint_as_float(v[8 * q + 7]));
-          dst[q] = o;
+        for (int r = 0; r < 4; ++r) {
+          if (lane == 0) bulk_wait_group_read0();  // the previous store has read the box
+          __syncwarp();
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            const int q = 4 * r + j;
+            uint4 o;
+            o.x = pack_bf16x2(__uint_as_float(v[8 * q + 0]), __uint_as_float(v[8 * q + 1]));
+            o.y = pack_bf16x2(__uint_as_float(v[8 * q + 2]), __uint_as_float(v[8 * q + 3]));
+            o.z = pack_bf16x2(__uint_as_float(v[8 * q + 4]), __uint_as_float(v[8 * q + 5]));
+            o.w = pack_bf16x2(__uint_as_float(v[8 * q + 6]), __uint_as_float(v[8 * q + 7]));
+            // 64-byte rows, 16-byte chunk j at j ^ (row / 2 % 4)
+            *reinterpret_cast<uint4*>(stg + lane * 64 + ((j ^ ((lane >> 1) & 3)) << 4)) = o;
+          }
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) {
+            tma_store_2d(&tmap_y, stg, (col0 + 32 * r) * 2, tc.m * kBM + qd * 32);
+            bulk_commit_group();
+          }
         }
       }
     }
+    if (lane == 0) bulk_wait_group0();  // every store has landed
   }
 
   tc_fence_before();
@@ -824,11 +879,11 @@ __global__ void __launch_bounds__(kMxThreads, 1)
 }
 
 template <int MODE>
-cudaError_t launch_mx(const CUtensorMap& tmap_a, const CUtensorMap& tmap_b, const LargeParams& p, int ctas,
-                      cudaStream_t stream) {
+cudaError_t launch_mx(const CUtensorMap& tmap_a, const CUtensorMap& tmap_b, const CUtensorMap& tmap_y,
+                      const LargeParams& p, int ctas, cudaStream_t stream) {
   cudaError_t e = ensure_smem_attr(reinterpret_cast<const void*>(&large_mx_kernel<MODE>), MxCfg<MODE>::SMEM);
   if (e != cudaSuccess) return e;
-  large_mx_kernel<MODE><<<ctas, kMxThreads, MxCfg<MODE>::SMEM, stream>>>(tmap_a, tmap_b, p);
+  large_mx_kernel<MODE><<<ctas, kMxThreads, MxCfg<MODE>::SMEM, stream>>>(tmap_a, tmap_b, tmap_y, p);
   return cudaGetLastError();
 }
 
@@ -1144,20 +1199,20 @@ uint64_t large_streamk_bytes(int ctas, bool wide) {
 
 bool large_supported(int mode) { return mode == kBF16 || mode == kTensor || mode == kBlock || is_mx(mode); }
 
-cudaError_t launch_large(int mode, const CUtensorMap& tmap_a, const CUtensorMap& tmap_b, const LargeParams& p,
-                         int ctas, cudaStream_t stream) {
+cudaError_t launch_large(int mode, const CUtensorMap& tmap_a, const CUtensorMap& tmap_b, const CUtensorMap& tmap_y,
+                         const LargeParams& p, int ctas, cudaStream_t stream) {
   if (p.wide) {
-    if (mode == kBF16) return launch_wide<kBF16>(tmap_a, p, ctas, stream);
-    if (mode == kTensor) return launch_wide<kTensor>(tmap_a, p, ctas, stream);
+    if (mode == kBF16) return launch_wide<kBF16>(tmap_a, tmap_y, p, ctas, stream);
+    if (mode == kTensor) return launch_wide<kTensor>(tmap_a, tmap_y, p, ctas, stream);
     return cudaErrorNotSupported;
   }
-  if (mode == kBlock) return launch_block(tmap_a, tmap_b, p, ctas, stream);  // tmap_b: the output's map
-  if (mode == kBF16) return launch_mode<kBF16>(tmap_a, p, ctas, stream);
-  if (mode == kTensor) return launch_mode<kTensor>(tmap_a, p, ctas, stream);
-  if (mode == kMXFP8) return launch_mx<kMXFP8>(tmap_a, tmap_b, p, ctas, stream);
-  if (mode == kMXFP8B32) return launch_mx<kMXFP8B32>(tmap_a, tmap_b, p, ctas, stream);
-  if (mode == kMXFP4) return launch_mx<kMXFP4>(tmap_a, tmap_b, p, ctas, stream);
-  if (mode == kMXFP4FP8A) return launch_mx<kMXFP4FP8A>(tmap_a, tmap_b, p, ctas, stream);
+  if (mode == kBlock) return launch_block(tmap_a, tmap_y, p, ctas, stream);
+  if (mode == kBF16) return launch_mode<kBF16>(tmap_a, tmap_y, p, ctas, stream);
+  if (mode == kTensor) return launch_mode<kTensor>(tmap_a, tmap_y, p, ctas, stream);
+  if (mode == kMXFP8) return launch_mx<kMXFP8>(tmap_a, tmap_b, tmap_y, p, ctas, stream);
+  if (mode == kMXFP8B32) return launch_mx<kMXFP8B32>(tmap_a, tmap_b, tmap_y, p, ctas, stream);
+  if (mode == kMXFP4) return launch_mx<kMXFP4>(tmap_a, tmap_b, tmap_y, p, ctas, stream);
+  if (mode == kMXFP4FP8A) return launch_mx<kMXFP4FP8A>(tmap_a, tmap_b, tmap_y, p, ctas, stream);
   return cudaErrorNotSupported;
 }
 
