@@ -223,7 +223,7 @@ fg_status make_plan(int mode, int64_t M, int64_t N, int64_t K, int split_k, fg_p
     out->stage_slabs = 1;
     if (large_pair(mode, M, N)) {
       out->tile_m = 256;
-      out->stages = 6;
+      out->stages = 5;
       const int64_t tiles = ((M + 255) / 256) * ((N + 255) / 256);
       const int64_t clusters = pair_max_clusters();
       out->ctas = static_cast<int32_t>(2 * (tiles < clusters ? tiles : clusters));
@@ -683,7 +683,9 @@ fg_status fg_gemm(const void* A, const void* a_scales, int64_t M, const fg_bshuf
                                 st);
     if (e != cudaSuccess) return cuda_fail(e, "A scale relayout launch");
     p.a_sf = static_cast<const uint8_t*>(workspace);
-    e = launch_large_pair(mode, tmap, tmap_b, tmap_asf, tmap_bsf, p, plan.ctas, st);
+    CUtensorMap tmap_y;
+    if ((s = make_tmap_out64(&tmap_y, Y, M, N)) != FG_OK) return s;
+    e = launch_large_pair(mode, tmap, tmap_b, tmap_asf, tmap_bsf, tmap_y, p, plan.ctas, st);
     if (e != cudaSuccess) return cuda_fail(e, "large-M pair kernel launch");
     return FG_OK;
   }

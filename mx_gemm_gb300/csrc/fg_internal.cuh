@@ -97,12 +97,13 @@ bool large_supported(int mode);
 // count of one scale box (the atoms of one 128-row block and slab), and the
 // launch.  tmap_b: the weight image as 2 KiB rows of 8-byte elements (box 8
 // rows) or, for kMXFP4FP8A, the 3-D map above; tmap_asf / tmap_bsf: the A and
-// weight scale images as 512-byte rows (one atom each).
+// weight scale images as 512-byte rows (one atom each); tmap_y: Y as rows of
+// 2N bytes, boxes of 32 rows x 64 bytes, 64-byte swizzle (tensor stores).
 int pair_max_clusters();
 uint32_t pair_sf_box_rows(int mode);
 cudaError_t launch_large_pair(int mode, const CUtensorMap& tmap_a, const CUtensorMap& tmap_b,
-                              const CUtensorMap& tmap_asf, const CUtensorMap& tmap_bsf, const LargeParams& p,
-                              int ctas, cudaStream_t stream);
+                              const CUtensorMap& tmap_asf, const CUtensorMap& tmap_bsf, const CUtensorMap& tmap_y,
+                              const LargeParams& p, int ctas, cudaStream_t stream);
 // One-CTA large-M kernels.  tmap_b: the MXFP4_FP8A weight image's map
 // (unused otherwise).  tmap_y: the output Y as rows of 2N bytes; all these
 // kernels write their bf16 tiles by tensor store -- kBlock and the 256 x 256

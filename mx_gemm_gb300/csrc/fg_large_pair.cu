@@ -75,8 +75,9 @@ struct PairCfg {
   static constexpr int SFB_OFF = SFA_OFF + SFA_BYTES;
   static constexpr int STAGE_RAW = SFB_OFF + SFB_BYTES;
   static constexpr int STAGE_BYTES = (STAGE_RAW + 1023) / 1024 * 1024;
-  static constexpr int STAGES = 6;
-  static constexpr int SMEM = STAGES * STAGE_BYTES + 1024;
+  static constexpr int STAGES = 5;  // room beside the ring for the output staging boxes
+  static constexpr int OUT_BYTES = 8 * 32 * 64;  // per epilogue warp: a 32-row x 32-column bf16 staging box
+  static constexpr int SMEM = STAGES * STAGE_BYTES + OUT_BYTES + 1024;
   // bytes one weight slab counts: the packed fp4 block of fp8 x fp4, else 16 KiB
   static constexpr int B_TX = MODE == kMXFP4FP8A ? 8192 : kBBytes;
   // mxfp8: one atom holds four slabs' scales (copied at the first slab of each
@@ -88,7 +89,7 @@ struct PairCfg {
   __host__ __device__ static constexpr uint32_t cta_tx(bool sf_here) {
     return static_cast<uint32_t>(kABytes + B_TX + (sf_here ? SFA_BYTES + SFB_BYTES : 0));
   }
-  static_assert(SMEM <= 232448, "shared memory budget");
+  static_assert(SMEM + 1024 <= 232448, "shared memory budget (with the static barriers)");
   static_assert(256 + SF_BUFS * SF_COLS <= kTmemCols, "TMEM budget");
 };
 
@@ -108,7 +109,7 @@ template <int MODE>
 __global__ void __launch_bounds__(kThreads, 1)
     large_mx_pair_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_b,
                          const __grid_constant__ CUtensorMap tmap_asf, const __grid_constant__ CUtensorMap tmap_bsf,
-                         const LargeParams p) {
+                         const __grid_constant__ CUtensorMap tmap_y, const LargeParams p) {
   using C = PairCfg<MODE>;
   extern __shared__ uint8_t dsmem[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(dsmem) + 1023) & ~uintptr_t(1023));
@@ -269,6 +270,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     // column half (warp - 2) / 4 of the 256 accumulator columns
     const int qd = warp & 3;
     const int half = (warp - 2) >> 2;
+    // this warp's 32-row x 32-column bf16 staging box (64-byte swizzle)
+    uint8_t* stg = smem + C::STAGES * C::STAGE_BYTES + (warp - 2) * (32 * 64);
     int ti = 0;
     for (int t = pair; t < tiles; t += npairs, ++ti) {
       const bool w = mbar_wait(&accf_bar, ti & 1, T, p.err, 46);
@@ -288,21 +291,36 @@ __global__ void __launch_bounds__(kThreads, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive_remote(&acce_bar, 0);  // the pair's next tile may overwrite the accumulator
       const TileCoord tc = tile_coord(t, p.tiles_m, p.tiles_n, p.group_n);
-      const int row = tc.m * kTileM + static_cast<int>(rank) * 128 + qd * 32 + lane;
+      const int row0 = tc.m * kTileM + static_cast<int>(rank) * 128 + qd * 32;
       const int col0 = tc.n * kTileN + half * 128;
-      if (row < p.M && col0 < p.N) {
-        uint4* dst = reinterpret_cast<uint4*>(p.y + static_cast<size_t>(row) * p.N + col0);
+      if (col0 < p.N) {
+        // bf16 out through the staging box, 32 columns at a time, by tensor
+        // store (rows past M are not written)
 #pragma unroll
-        for (int q = 0; q < 16; ++q) {
-          uint4 o;
-          o.x = pack_bf16x2(__uint_as_float(v[8 * q + 0]), __uint_as_float(v[8 * q + 1]));
-          o.y = pack_bf16x2(__uint_as_float(v[8 * q + 2]), __uint_as_float(v[8 * q + 3]));
-          o.z = pack_bf16x2(__uint_as_float(v[8 * q + 4]), __uint_as_float(v[8 * q + 5]));
-          o.w = pack_bf16x2(__uint_as_float(v[8 * q + 6]), __uint_as_float(v[8 * q + 7]));
-          dst[q] = o;
+        for (int r = 0; r < 4; ++r) {
+          if (lane == 0) bulk_wait_group_read0();  // the previous store has read the box
+          __syncwarp();
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            const int q = 4 * r + j;
+            uint4 o;
+            o.x = pack_bf16x2(__uint_as_float(v[8 * q + 0]), __uint_as_float(v[8 * q + 1]));
+            o.y = pack_bf16x2(__uint_as_float(v[8 * q + 2]), __uint_as_float(v[8 * q + 3]));
+            o.z = pack_bf16x2(__uint_as_float(v[8 * q + 4]), __uint_as_float(v[8 * q + 5]));
+            o.w = pack_bf16x2(__uint_as_float(v[8 * q + 6]), __uint_as_float(v[8 * q + 7]));
+            // 64-byte rows, 16-byte chunk j at j ^ (row / 2 % 4)
+            *reinterpret_cast<uint4*>(stg + lane * 64 + ((j ^ ((lane >> 1) & 3)) << 4)) = o;
+          }
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) {
+            tma_store_2d(&tmap_y, stg, (col0 + 32 * r) * 2, row0);
+            bulk_commit_group();
+          }
         }
       }
     }
+    if (lane == 0) bulk_wait_group0();  // every store has landed
   }
 
   // ------------------------------------------------------------- teardown
@@ -338,7 +356,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 template <int MODE>
 cudaError_t launch_pair(const CUtensorMap& tmap_a, const CUtensorMap& tmap_b, const CUtensorMap& tmap_asf,
-                        const CUtensorMap& tmap_bsf, const LargeParams& p, int ctas, cudaStream_t stream) {
+                        const CUtensorMap& tmap_bsf, const CUtensorMap& tmap_y, const LargeParams& p, int ctas,
+                        cudaStream_t stream) {
   using C = PairCfg<MODE>;
   cudaError_t e = ensure_smem_attr(reinterpret_cast<const void*>(&large_mx_pair_kernel<MODE>), C::SMEM);
   if (e != cudaSuccess) return e;
@@ -354,7 +373,7 @@ cudaError_t launch_pair(const CUtensorMap& tmap_a, const CUtensorMap& tmap_b, co
   attr.val.clusterDim.z = 1;
   cfg.attrs = &attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, large_mx_pair_kernel<MODE>, tmap_a, tmap_b, tmap_asf, tmap_bsf, p);
+  return cudaLaunchKernelEx(&cfg, large_mx_pair_kernel<MODE>, tmap_a, tmap_b, tmap_asf, tmap_bsf, tmap_y, p);
 }
 
 }  // namespace
@@ -390,13 +409,13 @@ int pair_max_clusters() {
 uint32_t pair_sf_box_rows(int mode) { return mode == kMXFP4 ? 2u : 1u; }
 
 cudaError_t launch_large_pair(int mode, const CUtensorMap& tmap_a, const CUtensorMap& tmap_b,
-                              const CUtensorMap& tmap_asf, const CUtensorMap& tmap_bsf, const LargeParams& p,
-                              int ctas, cudaStream_t stream) {
+                              const CUtensorMap& tmap_asf, const CUtensorMap& tmap_bsf, const CUtensorMap& tmap_y,
+                              const LargeParams& p, int ctas, cudaStream_t stream) {
   switch (mode) {
-    case kMXFP8: return launch_pair<kMXFP8>(tmap_a, tmap_b, tmap_asf, tmap_bsf, p, ctas, stream);
-    case kMXFP8B32: return launch_pair<kMXFP8B32>(tmap_a, tmap_b, tmap_asf, tmap_bsf, p, ctas, stream);
-    case kMXFP4: return launch_pair<kMXFP4>(tmap_a, tmap_b, tmap_asf, tmap_bsf, p, ctas, stream);
-    case kMXFP4FP8A: return launch_pair<kMXFP4FP8A>(tmap_a, tmap_b, tmap_asf, tmap_bsf, p, ctas, stream);
+    case kMXFP8: return launch_pair<kMXFP8>(tmap_a, tmap_b, tmap_asf, tmap_bsf, tmap_y, p, ctas, stream);
+    case kMXFP8B32: return launch_pair<kMXFP8B32>(tmap_a, tmap_b, tmap_asf, tmap_bsf, tmap_y, p, ctas, stream);
+    case kMXFP4: return launch_pair<kMXFP4>(tmap_a, tmap_b, tmap_asf, tmap_bsf, tmap_y, p, ctas, stream);
+    case kMXFP4FP8A: return launch_pair<kMXFP4FP8A>(tmap_a, tmap_b, tmap_asf, tmap_bsf, tmap_y, p, ctas, stream);
     default: return cudaErrorNotSupported;
   }
 }
