@@ -57,6 +57,7 @@ WORKLOADS = {
     "fp8_tensor_decode_m32_k7168": _wl("fp8_tensor_decode_m32_k7168", 0, 2, "decode"),
     "large_fp8_block128_4096x16384x7168": _wl("large_fp8_block128_4096x16384x7168", 0, 1, "large"),
     "large_fp8_block128_4096x8192x7168": _wl("large_fp8_block128_4096x8192x7168", 0, 1, "large"),
+    "large_mxfp4_4096x8192x7168": _wl("large_mxfp4_4096x8192x7168", 0, 1, "large"),
     # fp8 activations against fp4 weights, on the MX shapes
     "mxfp4_fp8a_decode_n16384_k7168": _wl("mx_fp8a_fp4w_n16384_k7168", 0, 2, "decode"),
     "large_mxfp4_fp8a_4096x16384x7168": _wl("mx_fp8a_fp4w_n16384_k7168", 2, 1, "large"),

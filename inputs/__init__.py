@@ -207,6 +207,9 @@ WORKLOADS = {
     # half of it (still larger than L2): the case a full kernel profile takes
     "large_fp8_block128_4096x8192x7168": dict(
         idx=10, cases=[dict(mode="fp8_block128", M=4096, N=8192, K=7168, split_k=1)]),
+    # the same for mxfp4 (packed operands: 4096 x 16384 x 7168 is 201 MB of A, B and Y)
+    "large_mxfp4_4096x8192x7168": dict(
+        idx=11, cases=[dict(mode="mxfp4", M=4096, N=8192, K=7168, split_k=1)]),
     # 32 tokens: one 32-token tile per weight tile
     "fp8_tensor_decode_m32_k7168": dict(
         idx=8, cases=[dict(mode="fp8_tensor", M=32, N=n, K=7168, split_k=0) for n in (2048, 16384)]),
