@@ -154,12 +154,16 @@ struct TableRow {
 // N=16384 shape alone is fastest at split 1 with 2 x 5 stages (185 KB a CTA,
 // 19.4 us against 20.1 us at split 2, 2 x 3), but in the sequence that
 // footprint shut out the next launch and the step took 51.8 us against 49.6.
+// Nor may a row let three CTAs share an SM where its 256 CTAs (N=16384,
+// split 2) should spread two to an SM over all of them: FP8_BLOCK128 at
+// 1 x 4 stages (74 KB, 96 registers) measured 20.7 / 23.7 us (M=1 / 16)
+// against 19.5 / 20.8 at 1 x 5 (90 KB).
 const TableRow kTable[] = {
     {FG_FP8_TENSOR, 1, 2048, 7168, 8, 2, 3},     {FG_FP8_TENSOR, 16, 2048, 7168, 8, 2, 3},
     {FG_FP8_TENSOR, 1, 2048, 7168, 4, 2, 5},  // an explicit split of 4 at this shape (timed alone)
     {FG_FP8_TENSOR, 1, 16384, 7168, 2, 2, 3},    {FG_FP8_TENSOR, 16, 16384, 7168, 2, 2, 3},
     {FG_FP8_BLOCK128, 1, 2048, 7168, 8, 1, 4},   {FG_FP8_BLOCK128, 16, 2048, 7168, 8, 1, 4},
-    {FG_FP8_BLOCK128, 1, 16384, 7168, 2, 1, 4},  {FG_FP8_BLOCK128, 16, 16384, 7168, 2, 1, 4},
+    {FG_FP8_BLOCK128, 1, 16384, 7168, 2, 1, 5},  {FG_FP8_BLOCK128, 16, 16384, 7168, 2, 1, 5},
     {FG_MXFP8, 1, 2048, 7168, 8, 1, 5},          {FG_MXFP8, 16, 2048, 7168, 8, 1, 4},
     {FG_MXFP8, 1, 16384, 7168, 2, 1, 4},         {FG_MXFP8, 16, 16384, 7168, 2, 1, 4},
     {FG_MXFP4, 1, 2048, 7168, 8, 1, 4},          {FG_MXFP4, 16, 2048, 7168, 8, 1, 4},
@@ -202,6 +206,25 @@ int large_group_n(int mode) {
     if (g >= 1 && g <= 4096) return g;
   }
   return is_mx(mode) ? 4 : 16;
+}
+
+// bf16 / FP8_BLOCK128 decode: slabs per partial-ready commit, as log2 (each
+// slab still has its own TMEM partial; a commit stalls the MMA pipe for about
+// as long as five 128 x 16 MMAs).  Any of 1, 2, 4 is valid for every
+// instantiated pipeline: a group ends at most three slabs after a stage's
+// last slab, inside a stage the producer has already filled.  Pairs when the
+// grid is at most one CTA per SM (a latency-bound chain of a few slabs per
+// CTA: N = 2048, split 8 measured 2-3 % faster); one slab otherwise, since
+// a stage is released only when its group is done, which shortens a
+// streaming pipeline (N = 16384: pairs 3 % slower, groups of 4 20 % slower).
+// FG_DECODE_PGROUP=1|2|4 overrides it (sweep hook).
+int decode_pgroup_log(int64_t ctas) {
+  if (const char* ov = getenv("FG_DECODE_PGROUP")) {
+    if (strcmp(ov, "1") == 0) return 0;
+    if (strcmp(ov, "2") == 0) return 1;
+    if (strcmp(ov, "4") == 0) return 2;
+  }
+  return ctas <= sm_count() ? 1 : 0;
 }
 
 // Large-M MX on CTA pairs (256 x 256 tiles, two SMs per tile): built and
@@ -765,6 +788,7 @@ fg_status fg_gemm(const void* A, const void* a_scales, int64_t M, const fg_bshuf
   p.split = split;
   p.fused_reduce = fused ? 1 : 0;
   p.debug_stall = (flags & FG_FLAG_DEBUG_STALL) ? 1 : 0;
+  p.pgroup_log = decode_pgroup_log(plan.ctas);
   DecodeConfig cfg{mode, plan.stage_slabs, plan.stages, plan.tile_m};
   if (!decode_config_supported(cfg)) return fail(FG_ERR_INVALID_ARG, "no kernel for config %s", plan.name);
   dim3 grid(static_cast<unsigned>(N / 128), static_cast<unsigned>(split),

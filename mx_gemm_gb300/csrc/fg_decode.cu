@@ -176,6 +176,14 @@ __global__ void __launch_bounds__(kThreads, (DCfg<MODE, SPS, STAGES, TOK>::MIN_C
   const int nslab = q + (split < r ? 1 : 0);
   const int niter = (nslab + SPS - 1) / SPS;
   const uint64_t T = p.timeout_ns;
+  // Per-slab partial modes: slab i's partial is announced by one commit for
+  // its group of 2^pg slabs (the split's last group may be shorter), on
+  // barrier (i >> pg) mod (NBUF >> pg); fewer commits keep the MMA pipe busy.
+  static_assert(C::NBUF == 8, "partial barrier indexing");
+  const int pg = C::PROMOTE ? p.pgroup_log : 0;
+  const int pg_nlog = 3 - pg;
+  auto pf_bar = [&](int i) { return &pfull_bar[(i >> pg) & ((1 << pg_nlog) - 1)]; };
+  auto pf_par = [&](int i) { return static_cast<uint32_t>((i >> (pg + pg_nlog)) & 1); };
   // fused reduce: the stage buffer that holds split s's receive area
   auto recv_slot = [&](int s) {
     const int ns = q + (s < r ? 1 : 0);
@@ -236,7 +244,7 @@ __global__ void __launch_bounds__(kThreads, (DCfg<MODE, SPS, STAGES, TOK>::MIN_C
         // the partial of the last slab of stage it - STAGES (slab commits
         // arrive in order, so every earlier MMA of the stage is done too)
         const int s_last = (it - STAGES + 1) * SPS - 1;
-        ok = mbar_wait(&pfull_bar[s_last % C::NBUF], (s_last / C::NBUF) & 1, T, p.err, 1);
+        ok = mbar_wait(pf_bar(s_last), pf_par(s_last), T, p.err, 1);
       }
       if (!__all_sync(0xffffffffu, ok)) {
         if (lane == 0) abort_sh = 1;
@@ -317,7 +325,7 @@ __global__ void __launch_bounds__(kThreads, (DCfg<MODE, SPS, STAGES, TOK>::MIN_C
         if (itf >= 0 && it == niter) {
           if (C::PF_RELEASE) {
             const int s_last = (itf + 1) * SPS - 1;
-            mbar_wait(&pfull_bar[s_last % C::NBUF], (s_last / C::NBUF) & 1, T, p.err, 9);
+            mbar_wait(pf_bar(s_last), pf_par(s_last), T, p.err, 9);
           } else {
             mbar_wait(&empty_bar[niter % STAGES], (itf / STAGES) & 1, T, p.err, 9);
           }
@@ -397,7 +405,8 @@ __global__ void __launch_bounds__(kThreads, (DCfg<MODE, SPS, STAGES, TOK>::MIN_C
             }
           }
           if (C::PROMOTE) {
-            tc_commit(&pfull_bar[pb]);
+            // the last slab of a group (or of the split) announces the group
+            if (((slab_ctr + 1) & ((1 << pg) - 1)) == 0 || slab_ctr + 1 == nslab) tc_commit(pf_bar(slab_ctr));
             ++slab_ctr;
           }
         }
@@ -500,25 +509,32 @@ __global__ void __launch_bounds__(kThreads, (DCfg<MODE, SPS, STAGES, TOK>::MIN_C
       for (int m = 0; m < kTokRows; ++m) comp[m] = 0.f;
       const float* a_s = static_cast<const float*>(p.a_scales);
       const int KS = p.K / 128;
+      // FP8_BLOCK128 scales of a slab: lane m holds token row m's a_s[row][kb]
+      // (one load per lane, shuffled to every lane in the fold) and every lane
+      // the weight tile's b_s[nb][kb]; both are loaded one slab ahead.
+      const int arow = mt * kTokRows + lane;
+      const bool arow_ok = MODE == kBlock && lane < kTokRows && arow < p.M;
+      const float* a_srow = arow_ok ? a_s + static_cast<size_t>(arow) * KS + u0 : nullptr;
+      const float* b_srow = MODE == kBlock ? p.b_s + static_cast<size_t>(nt) * KS + u0 : nullptr;
+      float a_next = 0.f, b_next = 0.f;
+      if (MODE == kBlock) {
+        a_next = arow_ok ? ld_nc_f32(a_srow) : 0.f;
+        b_next = ld_nc_f32(b_srow);
+      }
 #pragma unroll 1
       for (int i = 0; i < nslab; ++i) {
         const int pb = i % C::NBUF;
-        // the slab's scales are loaded before the wait for its MMA, so their
-        // latency hides behind it
-        const int kb = u0 + i;
-        float w_s[kTokRows];
-        if (MODE == kBlock) {
-          const float bsc = __ldg(p.b_s + static_cast<size_t>(nt) * KS + kb);
-#pragma unroll
-          for (int m = 0; m < kTokRows; ++m) {
-            const int row = mt * kTokRows + m;
-            w_s[m] = (row < p.M ? __ldg(a_s + static_cast<size_t>(row) * KS + kb) : 0.f) * bsc;
-          }
+        const float a_cur = a_next, bsc = b_next;
+        if (MODE == kBlock && i + 1 < nslab) {
+          a_next = arow_ok ? ld_nc_f32(a_srow + i + 1) : 0.f;
+          b_next = ld_nc_f32(b_srow + i + 1);
         }
-        const bool w = mbar_wait(&pfull_bar[pb], (i / C::NBUF) & 1, T, p.err, 5);
-        if (!__all_sync(0xffffffffu, w)) {
-          ok = false;
-          break;
+        if ((i & ((1 << pg) - 1)) == 0) {  // the first slab of a group waits for the whole group
+          const bool w = mbar_wait(pf_bar(i), pf_par(i), T, p.err, 5);
+          if (!__all_sync(0xffffffffu, w)) {
+            ok = false;
+            break;
+          }
         }
         tc_fence_after();
         uint32_t v[kTokRows];
@@ -530,7 +546,7 @@ __global__ void __launch_bounds__(kThreads, (DCfg<MODE, SPS, STAGES, TOK>::MIN_C
 #pragma unroll
         for (int m = 0; m < kTokRows; ++m) {
           float term = __uint_as_float(v[m]);
-          if (MODE == kBlock) term *= w_s[m];
+          if (MODE == kBlock) term *= __shfl_sync(0xffffffffu, a_cur, m) * bsc;
           const float yk = term - comp[m];
           const float t = acc[m] + yk;
           comp[m] = (t - acc[m]) - yk;

@@ -39,6 +39,7 @@ struct DecodeParams {
   int split;
   int fused_reduce;        // split > 1: the split CTAs of a tile form a cluster and reduce in DSMEM
   int debug_stall;
+  int pgroup_log;          // bf16 / FP8_BLOCK128: one partial-ready commit per 2^pgroup_log slabs (0..2)
 };
 
 struct DecodeConfig {

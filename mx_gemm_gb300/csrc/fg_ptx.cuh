@@ -138,6 +138,15 @@ __device__ __forceinline__ void prefetch_l2_box(const CUtensorMap* map, int32_t 
                "r"(x), "r"(y)
                : "memory");
 }
+// Read-only global load that stays where it is written: a volatile asm is
+// not moved past the barrier waits around it, so a value loaded ahead of a
+// wait is in flight during the wait (the compiler may sink a plain read-only
+// load to its first use).
+__device__ __forceinline__ float ld_nc_f32(const float* g) {
+  float v;
+  asm volatile("ld.global.nc.f32 %0, [%1];" : "=f"(v) : "l"(g));
+  return v;
+}
 __device__ __forceinline__ void prefetch_tmap(const CUtensorMap* map) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }
