@@ -395,3 +395,33 @@ def test_32_token_bounded_wait_reports_timeout():
             fg.set_wait_timeout_ns(4_000_000_000)
         assert fg.get_error() == fg.FG_OK
         parity.assert_y_close(y_to_f64(c.gemm(split_k=2)), c.ref(), f"{mode} 32 tokens after timeout")
+
+
+# ---------------------------------------- partial commits in groups of slabs
+
+@pytest.mark.parametrize("mode", ["fp8_block128", "bf16"])
+@pytest.mark.parametrize("group", ["1", "2", "4"])
+@pytest.mark.parametrize("cfg", ["1,4", "1,5", "2,3", "2,5", "4,2"])
+def test_partial_commit_groups(mode, group, cfg, monkeypatch):
+    """bf16 and blockscale announce their per-slab TMEM partials with one
+    commit per group of 1, 2 or 4 slabs (FG_DECODE_PGROUP); forced for each
+    pipeline, including 2 x 5, whose stages are released by their own
+    commits, and splits whose slab counts leave a short last group.  Every
+    output against the oracle, the fp32 partials against the workspace
+    bound, and the same bits as the default grouping (the sums do not depend
+    on when a partial is announced)."""
+    M, N, K = 5, 256, 3072
+    c = Case(mode, *inputs.operands(mode, M, N, K, 730, 731, 732))
+    ref = c.ref()
+    monkeypatch.setenv("FG_DECODE_CONFIG", cfg)
+    base = {S: c.gemm(split_k=S) for S in (1, 3, 7)}
+    monkeypatch.setenv("FG_DECODE_PGROUP", group)
+    for S in (1, 3, 7):
+        y = c.gemm(split_k=S)
+        parity.assert_y_close(y_to_f64(y), ref, f"{mode} {cfg} group {group} S={S}")
+        assert torch.equal(y.view(torch.int16), base[S].view(torch.int16))
+    parity.assert_ws_close(c.partials(3), c.ref_ws(3), f"{mode} {cfg} group {group} ws")
+    if cfg.startswith("1,"):   # 32-token tiles: one slab per stage
+        c32 = Case(mode, *inputs.operands(mode, 29, N, K, 733, 734, 735))
+        parity.assert_y_close(y_to_f64(c32.gemm(split_k=3)), c32.ref(), f"{mode} {cfg} group {group} 32 tokens")
+    assert fg.get_error() == fg.FG_OK
