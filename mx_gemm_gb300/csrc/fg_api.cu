@@ -293,6 +293,18 @@ fg_status make_plan(int mode, int64_t M, int64_t N, int64_t K, int split_k, fg_p
     const int64_t want = (static_cast<int64_t>(sm_count()) * 3) / 2;
     split = 1;
     while (split < 8 && tiles_n * tiles_m * split < want && KB / (split * 2) >= 4) split *= 2;
+    // fp8 per-tensor and blockscale CTAs of 1 x 4 stages (74 KB, few
+    // registers) fit three to an SM.  Where the grid needs between one and two
+    // CTAs per SM and each streams a long K range, that lets CTAs pile up
+    // three to an SM while others hold one; 1 x 5 (90 KB) keeps two to an SM.
+    // Measured (M = 1 / 16, K = 7168): N = 8192 split 4 11.9 / 12.5 us at 1 x 4
+    // against 11.1 / 11.5 at 1 x 5; with more CTAs than two per SM hold
+    // (N = 12288, K = 5120: 384 CTAs) or a few slabs per CTA (K = 2048 or
+    // 4096) 1 x 4 stays ahead (11.4 against 15.5 us; 4.6 against 5.1).
+    const int64_t ctas = tiles_n * tiles_m * split;
+    if ((mode == FG_FP8_TENSOR || mode == FG_FP8_BLOCK128) && tok == 16 && ctas > sm_count() &&
+        ctas <= 2 * static_cast<int64_t>(sm_count()) && KB / split >= 12)
+      stages = 5;
   }
   // Sweep hook: FG_DECODE_CONFIG="<slabs per stage>,<stages>" overrides the
   // pipeline shape of every decode launch (refused when not instantiated).

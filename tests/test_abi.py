@@ -91,6 +91,14 @@ def test_plan_heuristic_and_table(fg):
     assert p["split_k"] == 2 and (p["stage_slabs"], p["stages"]) == (2, 3) and p["from_table"]
     p = fg.gemm_plan("fp8_tensor", 8, 4096, 4096)          # heuristic: >= 1.5 CTAs per SM
     assert not p["from_table"] and p["ctas"] >= 1.5 * 148
+    # heuristic pipeline: 1 x 5 (two fp8 CTAs to an SM) when the grid needs one
+    # to two CTAs per SM and each streams >= 12 slabs, 1 x 4 otherwise
+    for mode, M, N, K, cfg in [("fp8_tensor", 16, 8192, 7168, (1, 5)), ("fp8_block128", 1, 8192, 7168, (1, 5)),
+                               ("fp8_tensor", 1, 12288, 5120, (1, 4)), ("fp8_tensor", 1, 4096, 4096, (1, 4)),
+                               ("fp8_tensor", 16, 16384, 2048, (1, 4)), ("mxfp8", 16, 8192, 7168, (1, 4)),
+                               ("fp8_tensor", 20, 8192, 7168, (1, 4))]:
+        p = fg.gemm_plan(mode, M, N, K)
+        assert not p["from_table"] and (p["stage_slabs"], p["stages"]) == cfg, (mode, M, N, K, p)
     p = fg.gemm_plan("fp8_tensor", 1, 2048, 7168, split_k=4)   # the row for an explicit split of 4
     assert p["split_k"] == 4 and p["from_table"] and (p["stage_slabs"], p["stages"]) == (2, 5)
     p = fg.gemm_plan("fp8_tensor", 1, 2048, 7168, split_k=2)   # a split no row has: the heuristic pipeline
