@@ -197,6 +197,21 @@ def test_decode_workload_parity(mode, M, N):
     parity.assert_y_close(y, ref, f"{mode} {M}x{N}")
 
 
+@pytest.mark.parametrize("mode", ["fp8_tensor", "fp8_block128"])
+@pytest.mark.parametrize("M", [1, 16])
+def test_heuristic_two_per_sm_pipeline(mode, M):
+    """A shape without a dispatch-table row whose grid needs one to two CTAs
+    per SM with a long K range: the heuristic takes split 4 with 1 x 5
+    stages; the fp32 partials at the workspace bound and every output."""
+    N, K = 8192, 7168
+    plan = fg.gemm_plan(mode, M, N, K)
+    assert not plan["from_table"] and plan["split_k"] == 4 and (plan["stage_slabs"], plan["stages"]) == (1, 5)
+    c = Case(mode, *inputs.operands(mode, M, N, K, 1100 + M, 2100, 3100))
+    parity.assert_ws_close(c.partials(4), c.ref_ws(4), f"{mode} {M}x{N} ws")
+    parity.assert_y_close(y_to_f64(c.gemm()), c.ref(), f"{mode} {M}x{N}")
+    assert fg.get_error() == fg.FG_OK
+
+
 def test_c1_split4_parity():
     """The first of the pages' decode configurations as stated: fp8
     per-tensor, M=1, N=2048, K=7168 with split_k fixed at 4 (not the
