@@ -122,8 +122,9 @@ struct DCfg {
       TMEM_NEED <= 32 ? 32 : (TMEM_NEED <= 64 ? 64 : (TMEM_NEED <= 128 ? 128 : (TMEM_NEED <= 256 ? 256 : 512)));
   static constexpr int SMEM = STAGES * STAGE_BYTES + 1024;
   // CTAs per SM the registers must leave room for: FP8 blockscale with 32
-  // tokens folds three 32-wide register arrays per slab and would otherwise
-  // take every register, leaving no room beside it for the next launch
+  // tokens folds 32-wide register arrays (the sums, their compensation, the
+  // slab's partial) and would otherwise take every register, leaving no room
+  // beside it for the next launch
   static constexpr int MIN_CTAS = (MODE == kBlock && TOK == 32) ? 2 : 1;
   static_assert(TMEM_NEED <= 512, "TMEM budget");
   static_assert(TOK == 16 || TOK == 32, "token tile");
